@@ -1,0 +1,209 @@
+/*
+ * b2pa.h -- C ABI of a batched paged-KV context (prefill) attention library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the FlashInfer API reference describes for
+ * flashinfer.prefill.trtllm_batch_context_with_kv_cache (parameter list:
+ * query, kv_cache, block_tables, seq_lens, max_q_len, max_kv_len,
+ * bmm1_scale, bmm2_scale, cum_seq_lens_q, cum_seq_lens_kv, window_left,
+ * kv_layout, sinks, out).  For every request b with q_len = cum_q[b+1] -
+ * cum_q[b] query tokens and kv_len = seq_lens[b] keys, query i (0 <= i <
+ * q_len) sits at position pos = kv_len - q_len + i (the queries are the
+ * last q_len tokens of the sequence, as the TokenSpeed trtllm backend's
+ * _init_extend_metadata builds them) and sees keys j with lo <= j <= pos,
+ * lo = 0 if window_left < 0 else max(0, pos - window_left).  Query head h
+ * reads kv head h / (H / Hkv).  With s_j = bmm1_scale * <q, K_j> and
+ * m = max_j s_j:
+ *
+ *   out = bmm2_scale * sum_j e^{s_j - m} V_j / (sum_j e^{s_j - m} + [sinks] e^{sinks[h] - m})
+ *
+ * Key j of request b is slot j % page_size of page block_tables[b][j /
+ * page_size] (TensorRT-LLM teardown (6), "Attention Backend 的 prepare()
+ * 内部", section "句柄到偏移的物理含义": the table holds page ids and the
+ * kernel adds id x page stride to the pool base).
+ *
+ * Conventions for every entry point:
+ *  - All tensors are described by b2pa_tensor: a pointer, a dtype, a rank,
+ *    and shape/stride arrays in ELEMENTS.  Tensors are owned by the caller;
+ *    the library never frees or keeps them past the call.
+ *  - Device tensors live on the current CUDA device; all work is enqueued on
+ *    `stream` in stream order.  Entry points that return results to the host
+ *    (b2pa_debug_worklist, b2pa_get_device_status) synchronise that stream.
+ *  - Return value: B2PA_OK (0) or a negative b2pa_status.  Argument errors
+ *    are detected on the host before anything is enqueued.  Problems that
+ *    only the device can see (a malformed request, a page id outside the
+ *    pool, a wait that timed out) never trap: the kernels skip the affected
+ *    work and OR a bit into a device error word, which
+ *    b2pa_get_device_status reads and clears.
+ *  - Thread safety: calls on different streams use separate workspaces and
+ *    may run concurrently; calls on one stream are ordered by the stream.
+ */
+#ifndef B2PA_H
+#define B2PA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define B2PA_API __attribute__((visibility("default")))
+#else
+#define B2PA_API
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st* b2pa_stream_t;
+
+enum b2pa_dtype {
+    B2PA_BF16 = 1,      /* bfloat16 */
+    B2PA_FP8_E4M3 = 2,  /* OCP FP8 E4M3 (float8_e4m3fn) */
+    B2PA_FP32 = 3,
+    B2PA_INT32 = 4
+};
+
+/* Which dims of a 4-D pool are page_size and num_kv_heads
+ * (FlashInfer API reference, parameter kv_layout). */
+enum b2pa_layout {
+    B2PA_HND = 0, /* [num_pages, num_kv_heads, page_size, head_dim] */
+    B2PA_NHD = 1  /* [num_pages, page_size, num_kv_heads, head_dim] */
+};
+
+enum b2pa_status {
+    B2PA_OK = 0,
+    B2PA_ERR_INVALID_ARG = -1, /* null pointer, bad rank/shape/dtype/stride, H % Hkv != 0, ... */
+    B2PA_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. a forced kernel path that cannot run the shape) */
+    B2PA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed; see b2pa_last_error_message */
+    B2PA_ERR_DEVICE = -4       /* b2pa_get_device_status: the device error word was non-zero */
+};
+
+/* Bits of the device error word (b2pa_get_device_status). */
+enum b2pa_device_error {
+    B2PA_DEV_BAD_REQUEST = 1,   /* q_len < 0, q_len > kv_len, q_len > max_q_len, kv_len > max_kv_len,
+                                   ceil(kv_len / page_size) > max_pages, or cum_q outside [0, num_tokens];
+                                   that request's rows are not written */
+    B2PA_DEV_BAD_PAGE = 2,      /* a page id a request reads is outside [0, num_pages); those keys read as 0 */
+    B2PA_DEV_TIMEOUT = 4,       /* a pipeline wait in a kernel gave up; the call's output is undefined */
+    B2PA_DEV_BAD_CUM_KV = 8,    /* cum_kv[b+1] - cum_kv[b] != seq_lens[b] (checked only where cum_kv is read) */
+    B2PA_DEV_OVERFLOW = 16      /* more work items than the workspace holds (cannot happen for valid bounds) */
+};
+
+/* Kernel paths (b2pa_set_kernel_path). */
+enum b2pa_path {
+    B2PA_PATH_AUTO = 0,    /* tensor-core path when the shape allows it, else the generic path */
+    B2PA_PATH_TCGEN05 = 1, /* TMA + tcgen05 tensor-core path only; B2PA_ERR_UNSUPPORTED if the shape does not fit */
+    B2PA_PATH_GENERIC = 2  /* CUDA-core path for any shape */
+};
+
+typedef struct {
+    void* data;         /* device pointer (host pointer where an entry point says so) */
+    int32_t dtype;      /* enum b2pa_dtype */
+    int32_t ndim;       /* 1..5 */
+    int64_t shape[5];   /* extents, outermost first */
+    int64_t stride[5];  /* strides in elements, outermost first */
+} b2pa_tensor;
+
+/*
+ * b2pa_context_attention -- batched context attention over a paged KV cache.
+ *
+ * Arguments (all device tensors):
+ *  q             [T, H, D] bf16; the ragged query tokens of all requests, request b
+ *                owning rows cum_q[b] .. cum_q[b+1]-1.  stride[2] must be 1.
+ *  k_pool,v_pool 4-D pools, same shape and dtype (bf16 or fp8 e4m3): [N, Hkv, P, D]
+ *                (B2PA_HND) or [N, P, Hkv, D] (B2PA_NHD); any strides with stride[3] == 1.
+ *                A single [N, 2, ...] cache is passed as its two strided views.
+ *  block_tables  [B, max_pages] int32, stride[1] == 1.  Entries past
+ *                ceil(seq_lens[b] / P) are never read.
+ *  seq_lens      [B] int32, kv length per request (cached prefix + new tokens).
+ *  cum_q         [B+1] int32, exclusive prefix sum of the query lengths.
+ *  cum_kv        [B+1] int32, exclusive prefix sum of seq_lens.  Not needed for
+ *                paged addressing; may be NULL.
+ *  max_q_len     upper bound on every q_len (sizes the work list).
+ *  max_kv_len    upper bound on every kv_len.
+ *  bmm1_scale    factor on Q K^T (e.g. k_scale / sqrt(D)); finite and > 0.
+ *  bmm2_scale    factor on the normalised P V (e.g. v_scale); finite.
+ *  window_left   -1 for full causal attention, else W >= 0: keys pos-W .. pos.
+ *  sinks         NULL, or [H] fp32: per query head, a logit (same units as
+ *                bmm1_scale * q.k) whose exponential joins the denominator.
+ *  layout        B2PA_HND or B2PA_NHD.
+ *  out           [T, H, D] bf16, caller allocated, stride[2] == 1.  Only rows of
+ *                valid requests are written.
+ *  stream        CUDA stream (NULL = legacy default stream).
+ *
+ * No host synchronisation.  Allocates (cudaMalloc) only when this stream's
+ * workspace must grow; once grown, the call can be captured in a CUDA graph.
+ */
+B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                           const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens,
+                           const b2pa_tensor* cum_q, const b2pa_tensor* cum_kv, int32_t max_q_len,
+                           int32_t max_kv_len, float bmm1_scale, float bmm2_scale, int32_t window_left,
+                           const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out,
+                           b2pa_stream_t stream);
+
+/*
+ * b2pa_debug_worklist -- run only the scheduler of the tensor-core path and
+ * copy its work list to the host (synchronises `stream`).
+ *
+ * Items are 4 int32 each: request b, kv head, item index it, cost.  Item it
+ * of request b covers query tokens [it * n_qtiles * rows_per_tile, ...) and
+ * cost = (kv tiles its rows touch) * (non-empty query tiles), sorted by
+ * min(cost, cost_cap) descending, ties in (b, kv head, it) order.
+ * geometry_out (may be NULL) receives {rows_per_tile, n_qtiles, kv_tile,
+ * cost_cap}.  host_items_out holds cap items; *n_out gets the count (which
+ * may exceed cap: only the first cap are copied).  Arguments as for
+ * b2pa_context_attention; k_pool supplies P, Hkv, D and dtype.
+ */
+B2PA_API int b2pa_debug_worklist(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* block_tables,
+                        const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q, int32_t max_q_len,
+                        int32_t max_kv_len, int32_t window_left, int32_t layout, int32_t* host_items_out,
+                        int32_t cap, int32_t* n_out, int32_t* geometry_out, b2pa_stream_t stream);
+
+/*
+ * b2pa_debug_gather -- copy the first seq_lens[b] logical K and V tokens of
+ * every request into contiguous k_out / v_out [sum(seq_lens), Hkv, D]
+ * (same dtype as the pools) at row offset cum_kv[b], through the same
+ * tensor-map page loads the attention kernel uses (the TensorRT-LLM Vanilla
+ * backend's _gather_paged_kv, TensorRT-LLM teardown (6), section
+ * "三条路径之一：VanillaAttention").  Requires a shape the tensor-core path
+ * supports (else B2PA_ERR_UNSUPPORTED).  cum_kv is required; k_out/v_out
+ * must be contiguous device tensors.
+ */
+B2PA_API int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
+                      const b2pa_tensor* seq_lens, const b2pa_tensor* cum_kv, int32_t layout,
+                      b2pa_tensor* k_out, b2pa_tensor* v_out, b2pa_stream_t stream);
+
+/*
+ * b2pa_get_device_status -- synchronise `stream`, read and clear the device
+ * error word of that stream's workspace.  Returns B2PA_OK if it was zero,
+ * else B2PA_ERR_DEVICE with the bits (enum b2pa_device_error) in *bits_out
+ * (may be NULL).
+ */
+B2PA_API int b2pa_get_device_status(b2pa_stream_t stream, uint32_t* bits_out);
+
+/* Choose the kernel path for later calls in this process (enum b2pa_path). */
+B2PA_API int b2pa_set_kernel_path(int32_t path);
+
+/* Which path b2pa_context_attention would take for these shapes (enum b2pa_path), or a negative status. */
+B2PA_API int b2pa_query_path(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                    const b2pa_tensor* out, int32_t layout);
+
+/* Turn on (1) / off (0) the extra device-side input checks: page ids against the pool and
+ * cum_kv against seq_lens.  Off by default. */
+B2PA_API int b2pa_set_debug_checks(int32_t on);
+
+/* Human-readable name of a b2pa_status. */
+B2PA_API const char* b2pa_status_string(int32_t status);
+
+/* Text of the last host-side error in this thread (empty if none). */
+B2PA_API const char* b2pa_last_error_message(void);
+
+/* Free every workspace this library allocated (all devices, all streams).  Must not be called while
+ * work that uses them is in flight. */
+B2PA_API void b2pa_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B2PA_H */

@@ -1,0 +1,262 @@
+"""Python binding of libb2pa.so: batched paged-KV context attention on GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/b2pa.h; this module turns torch
+tensors into b2pa_tensor descriptors and calls it.  There is no fallback:
+if the library is missing, load() raises.
+
+The call mirrors flashinfer.prefill.trtllm_batch_context_with_kv_cache
+(FlashInfer API reference, parameter list): ``query``, ``kv_cache`` (a
+(K, V) tuple or one [N, 2, ...] tensor), ``block_tables``, ``seq_lens``,
+``max_q_len``, ``max_kv_len``, ``bmm1_scale``, ``bmm2_scale``,
+``cum_seq_lens_q``, ``cum_seq_lens_kv``, ``window_left``, ``out``,
+``kv_layout`` and ``sinks``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libb2pa.so")
+
+B2PA_BF16, B2PA_FP8_E4M3, B2PA_FP32, B2PA_INT32 = 1, 2, 3, 4
+LAYOUTS = {"HND": 0, "NHD": 1}
+PATH_AUTO, PATH_TCGEN05, PATH_GENERIC = 0, 1, 2
+STATUS = {0: "B2PA_OK", -1: "B2PA_ERR_INVALID_ARG", -2: "B2PA_ERR_UNSUPPORTED", -3: "B2PA_ERR_CUDA",
+          -4: "B2PA_ERR_DEVICE"}
+DEV_BAD_REQUEST, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_CUM_KV, DEV_OVERFLOW = 1, 2, 4, 8, 16
+
+_DTYPES = {
+    torch.bfloat16: B2PA_BF16,
+    torch.float8_e4m3fn: B2PA_FP8_E4M3,
+    torch.float32: B2PA_FP32,
+    torch.int32: B2PA_INT32,
+}
+
+EXPORTED = [
+    "b2pa_context_attention",
+    "b2pa_debug_worklist",
+    "b2pa_debug_gather",
+    "b2pa_get_device_status",
+    "b2pa_set_kernel_path",
+    "b2pa_query_path",
+    "b2pa_set_debug_checks",
+    "b2pa_status_string",
+    "b2pa_last_error_message",
+    "b2pa_release",
+]
+
+
+class B2paTensor(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 5),
+        ("stride", ctypes.c_int64 * 5),
+    ]
+
+
+class B2paError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libb2pa.so (built by paged_kv_prefill_gb300.build); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with paged_kv_prefill_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(B2paTensor)
+    lib.b2pa_context_attention.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
+    lib.b2pa_context_attention.restype = ctypes.c_int
+    lib.b2pa_debug_worklist.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p]
+    lib.b2pa_debug_worklist.restype = ctypes.c_int
+    lib.b2pa_debug_gather.argtypes = [P, P, P, P, P, ctypes.c_int32, P, P, ctypes.c_void_p]
+    lib.b2pa_debug_gather.restype = ctypes.c_int
+    lib.b2pa_get_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.b2pa_get_device_status.restype = ctypes.c_int
+    lib.b2pa_set_kernel_path.argtypes = [ctypes.c_int32]
+    lib.b2pa_set_kernel_path.restype = ctypes.c_int
+    lib.b2pa_query_path.argtypes = [P, P, P, P, ctypes.c_int32]
+    lib.b2pa_query_path.restype = ctypes.c_int
+    lib.b2pa_set_debug_checks.argtypes = [ctypes.c_int32]
+    lib.b2pa_set_debug_checks.restype = ctypes.c_int
+    lib.b2pa_status_string.argtypes = [ctypes.c_int32]
+    lib.b2pa_status_string.restype = ctypes.c_char_p
+    lib.b2pa_last_error_message.argtypes = []
+    lib.b2pa_last_error_message.restype = ctypes.c_char_p
+    lib.b2pa_release.argtypes = []
+    lib.b2pa_release.restype = None
+    _lib = lib
+    return lib
+
+
+def desc(t: Optional[torch.Tensor]) -> Optional[B2paTensor]:
+    """b2pa_tensor describing a torch tensor (strides in elements)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 5:
+        raise ValueError("rank > 5")
+    d = B2paTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        msg = load().b2pa_last_error_message().decode()
+        raise B2paError(status, where, msg)
+
+
+def split_kv_cache(kv_cache, kv_layout: str) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(K, V) pools from a tuple or from one [N, 2, ...] tensor (its two strided views)."""
+    if isinstance(kv_cache, (tuple, list)):
+        k, v = kv_cache
+        return k, v
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2:
+        raise ValueError("a single kv_cache tensor must be [num_pages, 2, ...]; the shared K=V form is not supported")
+    return kv_cache[:, 0], kv_cache[:, 1]
+
+
+def context_attention(
+    query: torch.Tensor,
+    kv_cache: Union[torch.Tensor, Sequence[torch.Tensor]],
+    block_tables: torch.Tensor,
+    seq_lens: torch.Tensor,
+    max_q_len: int,
+    max_kv_len: int,
+    bmm1_scale: float,
+    bmm2_scale: float,
+    cum_seq_lens_q: torch.Tensor,
+    cum_seq_lens_kv: Optional[torch.Tensor] = None,
+    window_left: int = -1,
+    out: Optional[torch.Tensor] = None,
+    kv_layout: str = "HND",
+    sinks: Optional[torch.Tensor] = None,
+    stream=None,
+) -> torch.Tensor:
+    """Batched context attention over a paged KV cache (see include/b2pa.h)."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    if out is None:
+        out = torch.empty_like(query)
+    if isinstance(sinks, (list, tuple)):
+        if len(sinks) != 1:
+            raise ValueError("sinks: one fp32 [num_heads] tensor")
+        sinks = sinks[0]
+    dq, dk, dv, dbt, dsl, dcq = (desc(x) for x in (query, k, v, block_tables, seq_lens, cum_seq_lens_q))
+    dck, dsk, do = desc(cum_seq_lens_kv), desc(sinks), desc(out)
+    st = lib.b2pa_context_attention(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dbt), ctypes.byref(dsl),
+        ctypes.byref(dcq), _ref(dck), int(max_q_len), int(max_kv_len), float(bmm1_scale), float(bmm2_scale),
+        int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
+    )
+    _check(st, "b2pa_context_attention")
+    return out
+
+
+def debug_worklist(query, k_pool, block_tables, seq_lens, cum_seq_lens_q, max_q_len, max_kv_len,
+                   window_left=-1, kv_layout="HND", stream=None):
+    """Run the scheduler alone; returns (items int32 [n, 4] on the host, geometry dict)."""
+    import numpy as np
+
+    lib = load()
+    H = query.shape[1]
+    Hkv = k_pool.shape[1] if kv_layout == "HND" else k_pool.shape[2]
+    per = 2 * (128 // (H // Hkv))
+    cap = max(1, seq_lens.numel() * Hkv * ((max(max_q_len, 1) + per - 1) // per))
+    items = np.zeros((cap, 4), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    geo = (ctypes.c_int32 * 4)()
+    d = [desc(x) for x in (query, k_pool, block_tables, seq_lens, cum_seq_lens_q)]
+    st = lib.b2pa_debug_worklist(*(ctypes.byref(x) for x in d), int(max_q_len), int(max_kv_len), int(window_left),
+                                 LAYOUTS[kv_layout], items.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(n),
+                                 ctypes.byref(geo), ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "b2pa_debug_worklist")
+    geometry = {"rows_per_tile": geo[0], "n_qtiles": geo[1], "kv_tile": geo[2], "cost_cap": geo[3]}
+    return items[: min(n.value, cap)].copy(), geometry
+
+
+def debug_gather(kv_cache, block_tables, seq_lens, cum_seq_lens_kv, total_rows: int, kv_layout="HND", stream=None):
+    """Contiguous [total_rows, Hkv, D] K and V gathered through the kernel's page loads."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    Hkv = k.shape[1] if kv_layout == "HND" else k.shape[2]
+    D = k.shape[3]
+    k_out = torch.zeros((total_rows, Hkv, D), dtype=k.dtype, device=k.device)
+    v_out = torch.zeros_like(k_out)
+    d = [desc(x) for x in (k, v, block_tables, seq_lens, cum_seq_lens_kv)]
+    dko, dvo = desc(k_out), desc(v_out)
+    st = lib.b2pa_debug_gather(*(ctypes.byref(x) for x in d), LAYOUTS[kv_layout], ctypes.byref(dko),
+                               ctypes.byref(dvo), ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "b2pa_debug_gather")
+    return k_out, v_out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error bits of its workspace."""
+    lib = load()
+    bits = ctypes.c_uint32(0)
+    st = lib.b2pa_get_device_status(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(bits))
+    if st not in (0, -4):
+        _check(st, "b2pa_get_device_status")
+    return bits.value
+
+
+def set_kernel_path(path: Union[int, str]):
+    m = {"auto": PATH_AUTO, "tcgen05": PATH_TCGEN05, "generic": PATH_GENERIC}
+    _check(load().b2pa_set_kernel_path(m[path] if isinstance(path, str) else int(path)), "b2pa_set_kernel_path")
+
+
+def query_path(query, kv_cache, out=None, kv_layout="HND") -> str:
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    if out is None:
+        out = query
+    st = lib.b2pa_query_path(ctypes.byref(desc(query)), ctypes.byref(desc(k)), ctypes.byref(desc(v)),
+                             ctypes.byref(desc(out)), LAYOUTS[kv_layout])
+    if st < 0:
+        _check(st, "b2pa_query_path")
+    return {PATH_TCGEN05: "tcgen05", PATH_GENERIC: "generic"}[st]
+
+
+def set_debug_checks(on: bool):
+    load().b2pa_set_debug_checks(1 if on else 0)
+
+
+def release():
+    load().b2pa_release()

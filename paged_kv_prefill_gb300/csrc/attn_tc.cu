@@ -1,0 +1,759 @@
+// attn_tc.cu -- persistent, warp-specialised paged-KV context attention on
+// the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// What it computes is fixed by flashinfer.prefill.trtllm_batch_context_with_kv_cache
+// (FlashInfer API reference, parameter list) with the end-aligned causal
+// rule of the TokenSpeed trtllm backend (_init_extend_metadata); see the
+// header of include/b2pa.h.  The design below is ours.
+//
+// One CTA per SM loops over the scheduler's work list.  A work item is (request
+// b, kv head, item index): two query tiles of 128 MMA rows each, a row being
+// one (token, query head) pair of the kv head's group (rows_per_tile tokens x
+// G heads).  Both query tiles stream the same K/V tiles of 128 keys.
+//
+//   warp 0        producer: TMA loads of Q (3-D map) and of K/V pages (4-D
+//                 map, one box per page and 128-byte column block), through
+//                 a ring of shared-memory stages with full/empty mbarriers.
+//   warp 1        MMA issuer (one lane): S_t = Q_t K^T into TMEM, then
+//                 O_t += P_t V with P_t read from TMEM, for t = 0, 1,
+//                 interleaved so the tensor core works on one tile while
+//                 the other tile's softmax runs.  Owns the TMEM allocation.
+//   warps 4-7     softmax of query tile 0 (one thread per row), O rescale,
+//                 and the epilogue (bmm2_scale / denominator, bf16 stores).
+//   warps 8-11    the same for query tile 1.
+//   warps 12-15   (FP8 KV only) convert e4m3 K/V tiles to f16 in the MMA
+//                 layout, and the Q tile from bf16 to f16.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P_t (16-bit, two per column) overwrites the first 64 columns of S_t.
+//
+// Every wait is bounded: after kWaitLimitCycles the CTA raises
+// B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies and
+// MMAs are drained, and TMEM is freed before the CTA exits.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace b2pa {
+
+template <int D, bool FP8>
+struct TcCfg {
+    static constexpr int kHalves = D / 64;            // 128-byte column blocks per 16-bit row
+    static constexpr int kHalfBytes = kQRows * 128;   // one column block of a 128-row tile
+    static constexpr int kQTileBytes = kHalves * kHalfBytes;
+    static constexpr int kKvTileBytes = kHalves * kHalfBytes;
+    static constexpr int kStages = D == 128 ? (FP8 ? 3 : 4) : 8;
+    static constexpr int kF8Stages = FP8 ? 3 : 0;
+    static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
+    static constexpr int kThreads = FP8 ? 512 : 384;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kOCol = 2 * kKvTile;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffRing = kOffQ + kQTiles * kQTileBytes;
+    static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
+    static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 + 3 * kQTiles + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(!FP8 || D == 128, "fp8 path is D = 128");
+    static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
+};
+
+struct Bars {
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* f8full;
+    uint64_t* f8empty;
+    uint64_t* q_full;
+    uint64_t* q_empty;
+    uint64_t* q_conv;
+    uint64_t* s_full;
+    uint64_t* p_full;
+    uint64_t* o_full;
+    uint64_t* drain;
+};
+
+struct Ctx {
+    uint8_t* base;
+    Bars bar;
+    uint32_t tmem;
+    int n_items;
+    volatile int* abort_flag;
+};
+
+// Bounded wait on a barrier phase; false if this CTA gave up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity))
+        return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(a, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicOr(err, (unsigned)B2PA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait without looking at the abort flag (used when draining after an abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles)
+            return;
+    }
+}
+
+struct ItemInfo {
+    int b, kvh, q0, q_len, kv_len;
+    ItemGeom g;
+};
+
+__device__ __forceinline__ ItemInfo read_item(const AttnParams& p, int w)
+{
+    ItemInfo r;
+    const int4 it = p.items[w];
+    r.b = it.x;
+    r.kvh = it.y;
+    r.q0 = p.cum_q[r.b];
+    r.q_len = p.cum_q[r.b + 1] - r.q0;
+    r.kv_len = p.seq_lens[r.b];
+    r.g = item_geometry(r.q_len, r.kv_len, it.z, p.rows_per_tile, p.window);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Producer: warp 0.  Lane l loads page l of a kv tile (one TMA box per
+// 128-byte column block); lane 0 posts the byte count first.
+// ---------------------------------------------------------------------------
+template <int D, bool FP8>
+__device__ void producer_role(const AttnParams& p, const Ctx& c)
+{
+    using C = TcCfg<D, FP8>;
+    constexpr int kRingStages = FP8 ? C::kF8Stages : C::kStages;
+    constexpr int kRingTileBytes = FP8 ? C::kF8TileBytes : C::kKvTileBytes;
+    constexpr int kBoxes = FP8 ? 1 : C::kHalves;  // 128-byte-wide boxes per page
+    uint64_t* rfull = FP8 ? c.bar.f8full : c.bar.full;
+    uint64_t* rempty = FP8 ? c.bar.f8empty : c.bar.empty;
+    const int lane = threadIdx.x & 31;
+    const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
+    const uint32_t ring = smem_u32(c.base + (FP8 ? C::kOffF8 : C::kOffRing));
+    const int P = p.page_size;
+    const int ppt = P >= kKvTile ? 1 : kKvTile / P;  // pages per kv tile
+    const int box_rows = P >= kKvTile ? kKvTile : P;
+    const uint32_t q_box_bytes = (uint32_t)(p.G * p.rows_per_tile * 128);
+
+    uint32_t ring_idx = 0;
+    int item_iter = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
+        const ItemInfo it = read_item(p, w);
+        // Q tiles of this item (after the previous item's last Q K^T has read the buffer)
+        if (item_iter > 0 && !wait_bar(c.bar.q_empty, (item_iter - 1) & 1, c.abort_flag, p.err)) {
+            ok = false;
+            break;
+        }
+        if (lane == 0)
+            mbar_arrive_expect_tx(c.bar.q_full, (uint32_t)(it.g.nq * C::kHalves) * q_box_bytes);
+        __syncwarp();
+        if (lane < it.g.nq * C::kHalves) {
+            const int t = lane / C::kHalves, h = lane % C::kHalves;
+            tma_load_3d(q_smem + t * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, c.bar.q_full, h * 64,
+                        it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
+        }
+        const int* bt_row = p.block_tables + (long long)it.b * p.bt_stride;
+        const int n_pages_valid = (it.kv_len + P - 1) / P;
+        for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
+            const int first_col = (int)(((long long)j * kKvTile) / P);
+            const int slot0 = P > kKvTile ? (int)(((long long)j * kKvTile) % P) : 0;
+            const int col = first_col + lane;
+            const bool valid = lane < ppt && col < n_pages_valid;
+            const int page = valid ? bt_row[col] : 0;
+            if (valid && (page < 0 || page >= p.num_pages))
+                atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
+            const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+            const uint32_t bytes = nvalid * (uint32_t)box_rows * 128u * kBoxes;
+            for (int kind = 0; kind < 2; ++kind) {
+                const uint32_t s = ring_idx % kRingStages, ph = (ring_idx / kRingStages) & 1;
+                if (!wait_bar(&rempty[s], ph ^ 1, c.abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&rfull[s], bytes);
+                __syncwarp();
+                if (valid) {
+                    const uint32_t dst = ring + s * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
+#pragma unroll
+                    for (int h = 0; h < kBoxes; ++h)
+                        tma_load_4d(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &rfull[s], h * 64, slot0,
+                                    it.kvh, page);
+                }
+                ++ring_idx;
+            }
+        }
+    }
+    if (*c.abort_flag) {
+        // let the copies this warp started land before the CTA releases its memory
+        const uint32_t first = ring_idx > (uint32_t)kRingStages ? ring_idx - kRingStages : 0;
+        for (uint32_t k = first; k < ring_idx; ++k)
+            drain_wait(&rfull[k % kRingStages], (k / kRingStages) & 1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer: warp 1, lane 0 issues; the whole warp waits.
+// ---------------------------------------------------------------------------
+template <int D, bool FP8>
+__device__ void mma_role(const AttnParams& p, const Ctx& c)
+{
+    using C = TcCfg<D, FP8>;
+    // kind::f16; bf16 operands (f16 on the e4m3 path), f32 accumulators
+    constexpr uint32_t kFmt = FP8 ? 0u : 1u;
+    constexpr uint32_t kIdescS = (1u << 4) | (kFmt << 7) | (kFmt << 10) | ((uint32_t)(kKvTile >> 3) << 17) |
+                                 ((uint32_t)(kQRows >> 4) << 24);
+    constexpr uint32_t kIdescO = (1u << 4) | (kFmt << 7) | (kFmt << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) |
+                                 ((uint32_t)(kQRows >> 4) << 24);
+    const bool leader = (threadIdx.x & 31) == 0;
+    const int lane = threadIdx.x & 31;
+    const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
+    const uint32_t ring = smem_u32(c.base + C::kOffRing);
+    uint64_t* const full = c.bar.full;
+    uint64_t* const empty = c.bar.empty;
+
+    auto issue_s = [&](int t, uint32_t slot) {
+        const uint32_t a0 = q_smem + t * C::kQTileBytes;
+        const uint32_t b0 = ring + slot * C::kKvTileBytes;
+        const uint32_t d = c.tmem + (uint32_t)(t * kKvTile);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (uint32_t)((k / 4) * C::kHalfBytes + (k % 4) * 32);
+            mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS, k > 0 ? 1u : 0u);
+        }
+    };
+    auto issue_pv = [&](int t, uint32_t slot, bool acc) {
+        const uint32_t b0 = ring + slot * C::kKvTileBytes;
+        const uint32_t d = c.tmem + (uint32_t)(C::kOCol + t * D);
+        const uint32_t a = c.tmem + (uint32_t)(t * kKvTile);
+#pragma unroll
+        for (int k = 0; k < kKvTile / 16; ++k)
+            mma_ts(d, a + (uint32_t)(k * 8), sdesc_sw128(b0 + (uint32_t)(k * 16 * 128), C::kHalfBytes, 1024), kIdescO,
+                   (acc || k > 0) ? 1u : 0u);
+    };
+    auto wait_full = [&](uint32_t r) -> bool {
+        return wait_bar(&full[r % C::kStages], (r / C::kStages) & 1, c.abort_flag, p.err);
+    };
+
+    uint32_t ring_idx = 0;
+    uint32_t p_cnt[kQTiles] = {0, 0};
+    int item_iter = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
+        const ItemInfo it = read_item(p, w);
+        const int nq = it.g.nq;
+        if (!wait_bar(FP8 ? c.bar.q_conv : c.bar.q_full, item_iter & 1, c.abort_flag, p.err)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // S for the first kv tile
+        const uint32_t rk = ring_idx++;
+        if (!wait_full(rk)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        if (leader) {
+            for (int t = 0; t < nq; ++t) {
+                issue_s(t, rk % C::kStages);
+                mma_commit(&c.bar.s_full[t]);
+            }
+            mma_commit(&empty[rk % C::kStages]);
+            if (it.g.n_lo == it.g.n_hi)
+                mma_commit(c.bar.q_empty);
+        }
+        __syncwarp();
+        for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
+            const bool last = j == it.g.n_hi;
+            const uint32_t rv = ring_idx++;
+            const uint32_t rk2 = last ? 0u : ring_idx++;
+            if (!wait_full(rv)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (!FP8) {
+                // keys >= kv_len: V rows may hold any bits (or a page that was not
+                // loaded); zero them so that P = 0 there cannot meet a NaN.
+                const int k0 = j * kKvTile;
+                const int r0 = it.kv_len - k0;
+                if (r0 < kKvTile) {
+                    uint8_t* vt = c.base + C::kOffRing + (rv % C::kStages) * C::kKvTileBytes;
+                    const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        uint4* dst = reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + r0 * 128);
+                        for (int q = lane; q < n16; q += 32)
+                            dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
+            for (int t = 0; ok && t < nq; ++t) {
+                if (!wait_bar(&c.bar.p_full[t], p_cnt[t] & 1, c.abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                ++p_cnt[t];
+                tc_fence_after();
+                if (leader) {
+                    issue_pv(t, rv % C::kStages, j > it.g.n_lo);
+                    if (t == nq - 1)
+                        mma_commit(&empty[rv % C::kStages]);
+                    if (last)
+                        mma_commit(&c.bar.o_full[t]);
+                }
+                __syncwarp();
+                if (!last) {
+                    if (t == 0) {
+                        if (!wait_full(rk2)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (leader) {
+                        issue_s(t, rk2 % C::kStages);
+                        mma_commit(&c.bar.s_full[t]);
+                        if (t == nq - 1) {
+                            mma_commit(&empty[rk2 % C::kStages]);
+                            if (j + 1 == it.g.n_hi)
+                                mma_commit(c.bar.q_empty);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    }
+    (void)lane;
+    // every MMA this thread issued has completed once the drain barrier flips
+    if (leader)
+        mma_commit(c.bar.drain);
+    __syncwarp();
+    drain_wait(c.bar.drain, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax / correction / epilogue for query tile t: warps 4+4t .. 7+4t, one
+// thread per TMEM lane (= MMA row).
+// ---------------------------------------------------------------------------
+template <int D, bool FP8>
+__device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
+{
+    using C = TcCfg<D, FP8>;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const int wq = (threadIdx.x >> 5) & 3;
+    const int lane = threadIdx.x & 31;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t s_tmem = c.tmem + lane_off + (uint32_t)(t * kKvTile);
+    const uint32_t o_tmem = c.tmem + lane_off + (uint32_t)(C::kOCol + t * D);
+    const int G = p.G, Tq = p.rows_per_tile;
+    const int r_tok = row / G, r_head = row % G;
+    const bool row_real = row < G * Tq;
+    const float sl2 = p.scale_log2;
+
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x) {
+        const ItemInfo it = read_item(p, w);
+        if (t >= it.g.nq)
+            continue;
+        const int prefix = it.kv_len - it.q_len;
+        const int i_first = it.g.tok0 + t * Tq;
+        const int i = i_first + r_tok;
+        const bool valid = row_real && i < it.q_len;
+        const int pos = prefix + i;
+        const int lo = p.window < 0 ? 0 : max(0, pos - p.window);
+        const int hi = valid ? pos : -1;
+        const int i_last = min(i_first + Tq, it.q_len) - 1;
+        const int p_first = prefix + i_first, p_last = prefix + i_last;
+        const int lo_last = p.window < 0 ? 0 : max(0, p_last - p.window);
+
+        float m_used = -INFINITY;
+        float l = 0.f;
+        for (int j = it.g.n_lo; j <= it.g.n_hi; ++j) {
+            if (!wait_bar(&c.bar.s_full[t], s_cnt & 1, c.abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
+            ++s_cnt;
+            tc_fence_after();
+            float s[kKvTile];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    tmem_ld32(s_tmem + (uint32_t)(q * 32), r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        s[q * 32 + k] = __uint_as_float(r[k]);
+                }
+                tmem_wait_ld();
+            }
+            const int k0 = j * kKvTile;
+            const bool interior = k0 >= lo_last && k0 + kKvTile - 1 <= p_first;
+            if (!interior) {
+#pragma unroll
+                for (int k = 0; k < kKvTile; ++k) {
+                    const int key = k0 + k;
+                    if (key < lo || key > hi)
+                        s[k] = -INFINITY;
+                }
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int k = 1; k < kKvTile; ++k)
+                mx = fmaxf(mx, s[k]);
+            const float m_tile = mx * sl2;
+            // keep a stale maximum until the row maximum grows by more than 2^8:
+            // exact, since the denominator uses the same stale maximum
+            const bool need = m_tile > m_used + 8.0f;
+            float alpha = 1.f;
+            if (need) {
+                alpha = ex2_approx(m_used - m_tile);
+                l *= alpha;
+                m_used = m_tile;
+            }
+            const float neg = m_used == -INFINITY ? 0.f : -m_used;
+            float rs0 = 0.f, rs1 = 0.f;
+            uint32_t pk[kKvTile / 2];
+#pragma unroll
+            for (int k = 0; k < kKvTile / 2; ++k) {
+                const float p0 = ex2_approx(fmaf(s[2 * k], sl2, neg));
+                const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, neg));
+                rs0 += p0;
+                rs1 += p1;
+                if (FP8) {
+                    uint32_t r;
+                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));
+                    pk[k] = r;
+                } else {
+                    pk[k] = pack_bf16x2(p0, p1);
+                }
+            }
+            l += rs0 + rs1;
+            {
+                uint32_t (&pa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+                uint32_t (&pb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+                tmem_st32(s_tmem, pa);
+                tmem_st32(s_tmem + 32, pb);
+            }
+            if (__any_sync(0xffffffffu, need) && j > it.g.n_lo) {
+                const float a = need ? alpha : 1.f;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
+                    tmem_st32(o_tmem + (uint32_t)(q * 32), o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c.bar.p_full[t]);
+        }
+        if (!ok)
+            break;
+        // epilogue: out = bmm2_scale * O / (l + e^{sink - m})
+        if (!wait_bar(&c.bar.o_full[t], o_cnt & 1, c.abort_flag, p.err)) {
+            ok = false;
+            break;
+        }
+        ++o_cnt;
+        tc_fence_after();
+        const int h = it.kvh * G + r_head;
+        float total = l;
+        if (p.sinks != nullptr && m_used != -INFINITY && row_real)
+            total += ex2_approx(fmaf(p.sinks[h], kLog2e, -m_used));
+        const float inv = (m_used != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
+        uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
+            tmem_wait_ld();
+            if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 pk4;
+                    pk4.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    pk4.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    pk4.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    pk4.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    dst[v] = pk4;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+}
+
+// ---------------------------------------------------------------------------
+// e4m3 -> f16 conversion (FP8 KV path): warps 12-15, one thread per tile row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    uint32_t r;
+    const uint16_t h = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    const float lo = __uint_as_float(w << 16);
+    const float hi = __uint_as_float(w & 0xFFFF0000u);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <int D, bool FP8>
+__device__ void convert_role(const AttnParams& p, const Ctx& c)
+{
+    using C = TcCfg<D, FP8>;
+    const int ct = threadIdx.x - 12 * 32;  // 0..127: tile row
+    const int lane = threadIdx.x & 31;
+    const int sw = ct & 7;                 // 128-byte swizzle phase of this row
+    uint32_t r8 = 0, r = 0;
+    int item_iter = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
+        const ItemInfo it = read_item(p, w);
+        if (!wait_bar(c.bar.q_full, item_iter & 1, c.abort_flag, p.err)) {
+            ok = false;
+            break;
+        }
+        for (int t = 0; t < it.g.nq; ++t) {
+            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + t * C::kQTileBytes);
+            for (int k = ct; k < C::kQTileBytes / 16; k += 128) {
+                uint4 v = q[k];
+                v.x = bf16x2_to_f16x2(v.x);
+                v.y = bf16x2_to_f16x2(v.y);
+                v.z = bf16x2_to_f16x2(v.z);
+                v.w = bf16x2_to_f16x2(v.w);
+                q[k] = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(c.bar.q_conv);
+        for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
+            const bool zero = j * kKvTile + ct >= it.kv_len;
+            for (int kind = 0; kind < 2; ++kind) {
+                const uint32_t s8 = r8 % C::kF8Stages, s = r % C::kStages;
+                if (!wait_bar(&c.bar.f8full[s8], (r8 / C::kF8Stages) & 1, c.abort_flag, p.err) ||
+                    !wait_bar(&c.bar.empty[s], ((r / C::kStages) & 1) ^ 1, c.abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* src = c.base + C::kOffF8 + s8 * C::kF8TileBytes + ct * 128;
+                uint8_t* dst = c.base + C::kOffRing + s * C::kKvTileBytes + ct * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {  // 16 e4m3 values = d 16q .. 16q+15
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
+                    if (!zero) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
+                        lo.x = e4m3x2_to_f16x2(x.x);
+                        lo.y = e4m3x2_to_f16x2(x.x >> 16);
+                        lo.z = e4m3x2_to_f16x2(x.y);
+                        lo.w = e4m3x2_to_f16x2(x.y >> 16);
+                        hi.x = e4m3x2_to_f16x2(x.z);
+                        hi.y = e4m3x2_to_f16x2(x.z >> 16);
+                        hi.z = e4m3x2_to_f16x2(x.w);
+                        hi.w = e4m3x2_to_f16x2(x.w >> 16);
+                    }
+                    const int hb = q >> 2, cc = (2 * q) & 7;
+                    uint8_t* rowp = dst + hb * C::kHalfBytes;
+                    *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ sw) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&c.bar.full[s]);
+                    mbar_arrive(&c.bar.f8empty[s8]);
+                }
+                ++r8;
+                ++r;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <int D, bool FP8>
+__global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kernel(const __grid_constant__ AttnParams p)
+{
+    using C = TcCfg<D, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kOffBar);
+    Ctx c;
+    c.base = base;
+    c.bar.full = bars;
+    c.bar.empty = bars + C::kStages;
+    c.bar.f8full = c.bar.empty + C::kStages;
+    c.bar.f8empty = c.bar.f8full + C::kF8Stages;
+    c.bar.q_full = c.bar.f8empty + C::kF8Stages;
+    c.bar.q_empty = c.bar.q_full + 1;
+    c.bar.q_conv = c.bar.q_full + 2;
+    c.bar.s_full = c.bar.q_full + 3;
+    c.bar.p_full = c.bar.s_full + kQTiles;
+    c.bar.o_full = c.bar.p_full + kQTiles;
+    c.bar.drain = c.bar.o_full + kQTiles;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
+    c.abort_flag = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&c.bar.full[s], FP8 ? 4 : 1);
+            mbar_init(&c.bar.empty[s], 1);
+        }
+        for (int s = 0; s < C::kF8Stages; ++s) {
+            mbar_init(&c.bar.f8full[s], 1);
+            mbar_init(&c.bar.f8empty[s], 4);
+        }
+        mbar_init(c.bar.q_full, 1);
+        mbar_init(c.bar.q_empty, 1);
+        mbar_init(c.bar.q_conv, 4);
+        for (int t = 0; t < kQTiles; ++t) {
+            mbar_init(&c.bar.s_full[t], 1);
+            mbar_init(&c.bar.p_full[t], 4);
+            mbar_init(&c.bar.o_full[t], 1);
+        }
+        mbar_init(c.bar.drain, 1);
+        *c.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tmap(&p.tm_q);
+        prefetch_tmap(&p.tm_k);
+        prefetch_tmap(&p.tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::kTmemCols);
+        tmem_relinquish();
+    }
+    {
+        // Q rows past G * rows_per_tile are never written by TMA: keep them zero
+        const int used = p.G * p.rows_per_tile * 128;
+        const int pad = C::kHalfBytes - used;
+        if (pad > 0) {
+            const int n16 = pad / 16;
+            for (int k = threadIdx.x; k < kQTiles * C::kHalves * n16; k += blockDim.x) {
+                const int blk = k / n16, q = k % n16;
+                *reinterpret_cast<uint4*>(base + C::kOffQ + blk * C::kHalfBytes + used + q * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    c.tmem = *tmem_holder;
+
+    // the work list is written by the scheduler kernel that precedes this one
+    pdl_wait();
+    c.n_items = min(*p.count, p.cap);
+
+    if constexpr (FP8) {
+        // 512 threads launch with 128 registers each; the softmax warpgroups
+        // take registers from the others (56 + 184 + 184 + 80 = 504 <= 4 x 128)
+        if (warp < 4) {
+            regs_dec<56>();
+            if (warp == 0)
+                producer_role<D, FP8>(p, c);
+            else if (warp == 1)
+                mma_role<D, FP8>(p, c);
+        } else if (warp < 12) {
+            regs_inc<184>();
+            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+        } else {
+            regs_dec<80>();
+            convert_role<D, FP8>(p, c);
+        }
+    } else {
+        if (warp == 0)
+            producer_role<D, FP8>(p, c);
+        else if (warp == 1)
+            mma_role<D, FP8>(p, c);
+        else if (warp >= 4)
+            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(c.tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream, bool pdl)
+{
+    using C = TcCfg<D, FP8>;
+    auto kern = attention_tc_kernel<D, FP8>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl)
+{
+    if (fp8)
+        return head_dim == 128 ? launch_one<128, true>(p, grid, stream, pdl) : cudaErrorInvalidValue;
+    if (head_dim == 128)
+        return launch_one<128, false>(p, grid, stream, pdl);
+    if (head_dim == 64)
+        return launch_one<64, false>(p, grid, stream, pdl);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace b2pa

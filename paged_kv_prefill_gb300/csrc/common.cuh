@@ -1,0 +1,148 @@
+// common.cuh -- parameters, constants and the per-item geometry shared by
+// the scheduler, the tensor-core attention kernel and the debug gather.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/b2pa.h"
+
+namespace b2pa {
+
+constexpr int kKvTile = 128;      // keys per kv tile (MMA N of Q K^T, K of P V)
+constexpr int kQRows = 128;       // MMA M rows per query tile (tokens x heads of one kv group)
+constexpr int kQTiles = 2;        // query tiles per work item (they share every K/V tile)
+constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
+constexpr int kSchedBuckets = kCostCap + 1;
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedMaxBatch = 16384;
+constexpr long long kWaitLimitCycles = 1LL << 31;  // ~1 s at 2 GHz: a pipeline wait that exceeds this gives up
+
+// A request is processed only if its lengths are consistent with the bounds
+// the caller gave; otherwise the scheduler sets B2PA_DEV_BAD_REQUEST.
+struct RequestView {
+    int q_start;
+    int q_len;
+    int kv_len;
+    bool ok;
+};
+
+__device__ __forceinline__ RequestView load_request(const int* cum_q, const int* seq_lens, int b, int max_q_len,
+                                                    int max_kv_len, int page_size, int max_pages, int num_tokens)
+{
+    RequestView r;
+    int q0 = cum_q[b], q1 = cum_q[b + 1];
+    r.q_start = q0;
+    r.q_len = q1 - q0;
+    r.kv_len = seq_lens[b];
+    long long pages = ((long long)r.kv_len + page_size - 1) / page_size;
+    r.ok = r.q_len >= 0 && r.q_len <= r.kv_len && r.q_len <= max_q_len && r.kv_len <= max_kv_len &&
+           pages <= max_pages && q0 >= 0 && q1 <= num_tokens;
+    return r;
+}
+
+// Geometry of work item `it` of a request: which query tokens it covers and
+// which kv tiles their visible keys touch.  Query i sits at position
+// kv_len - q_len + i and sees keys lo(pos) .. pos, lo = 0 for a negative
+// window, else max(0, pos - window).
+struct ItemGeom {
+    int tok0;   // first query token (index within the request)
+    int nq;     // query tiles with at least one token (1 .. kQTiles)
+    int n_lo;   // first kv tile
+    int n_hi;   // last kv tile
+};
+
+__device__ __forceinline__ ItemGeom item_geometry(int q_len, int kv_len, int it, int rows_per_tile, int window)
+{
+    ItemGeom g;
+    const int per_item = rows_per_tile * kQTiles;
+    g.tok0 = it * per_item;
+    int i1 = min(g.tok0 + per_item, q_len) - 1;
+    g.nq = (i1 - g.tok0) / rows_per_tile + 1;
+    int prefix = kv_len - q_len;
+    int p_min = prefix + g.tok0, p_max = prefix + i1;
+    int lo = window < 0 ? 0 : max(0, p_min - window);
+    g.n_lo = lo / kKvTile;
+    g.n_hi = p_max / kKvTile;
+    return g;
+}
+
+struct SchedParams {
+    const int* cum_q;
+    const int* seq_lens;
+    const int* cum_kv;        // may be null
+    const int* block_tables;  // read only when debug != 0
+    long long bt_stride;
+    int B, Hkv, rows_per_tile, window, max_q_len, max_kv_len, page_size, max_pages, num_tokens, num_pages;
+    int debug;
+    int cap;
+    int4* items;
+    int* count;
+    unsigned* err;
+};
+
+struct AttnParams {  // 128-byte aligned through its CUtensorMap members
+    CUtensorMap tm_q;   // 3-D: (D, H, T), box (64, G, rows_per_tile)
+    CUtensorMap tm_k;   // 4-D: (D, P, Hkv, pages), box (64 | 128 bytes, min(P,128), 1, 1)
+    CUtensorMap tm_v;
+    const int* cum_q;
+    const int* seq_lens;
+    const int* block_tables;
+    const float* sinks;  // may be null
+    uint16_t* out;       // bf16 bits
+    long long bt_stride;
+    long long out_stride_tok;
+    long long out_stride_head;
+    const int4* items;
+    const int* count;
+    unsigned* err;
+    int cap;
+    int H, Hkv, G, rows_per_tile, page_size, num_pages;
+    int window;
+    float scale_log2;    // bmm1_scale * log2(e)
+    float bmm2;
+};
+
+struct GatherParams {
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    const int* seq_lens;
+    const int* cum_kv;
+    const int* block_tables;
+    long long bt_stride;
+    uint8_t* k_out;
+    uint8_t* v_out;
+    long long out_rows;
+    int B, Hkv, D, page_size, max_pages, num_pages, esize;
+    unsigned* err;
+};
+
+struct GenericParams {
+    const uint16_t* q;
+    const void* k;
+    const void* v;
+    const int* cum_q;
+    const int* seq_lens;
+    const int* block_tables;
+    const float* sinks;
+    uint16_t* out;
+    long long q_st_tok, q_st_head;
+    long long out_st_tok, out_st_head;
+    long long k_st_page, k_st_head, k_st_slot;  // element strides by logical dim
+    long long v_st_page, v_st_head, v_st_slot;
+    long long bt_stride;
+    int B, T, H, Hkv, D, page_size, max_pages, num_pages, max_q_len, max_kv_len;
+    int window;
+    float scale_log2;
+    float bmm2;
+    unsigned* err;
+};
+
+// Host launchers (one translation unit each).
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaStream_t stream);
+cudaError_t launch_attention_generic(const GenericParams& p, bool fp8, cudaStream_t stream);
+
+}  // namespace b2pa

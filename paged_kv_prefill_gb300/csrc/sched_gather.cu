@@ -1,0 +1,304 @@
+// sched_gather.cu -- the work-list scheduler of the tensor-core path and the
+// debug gather that exercises its paged K/V loads.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace b2pa {
+
+// ---------------------------------------------------------------------------
+// Scheduler: one CTA of 1024 threads.
+//
+// 1. Validate each request (load_request) and count its items:
+//    Hkv * ceil(q_len / (rows_per_tile * kQTiles)).
+// 2. Enumerate items in (b, kv head, it) order; cost = kv tiles x non-empty
+//    query tiles (item_geometry), bucket = min(cost, kCostCap).
+// 3. Stable counting sort by bucket, descending: each warp owns a contiguous
+//    slice of the enumeration, counts per bucket with __match_any_sync,
+//    bucket starts come from a scan over (bucket descending, warp ascending),
+//    and a second pass scatters each item to its rank.  The order is fully
+//    deterministic.
+// Writes items[0 .. n) and *count = n; sets B2PA_DEV_BAD_REQUEST for
+// rejected requests (their items are not emitted).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o)
+                s += y;
+        }
+        scratch[lane] = s;  // inclusive warp totals
+    }
+    __syncthreads();
+    const int before = warp > 0 ? scratch[warp - 1] : 0;
+    if (total)
+        *total = scratch[(blockDim.x >> 5) - 1];
+    const int r = before + x - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedParams p)
+{
+    // let the attention kernel start its prologue while the list is built
+    pdl_launch_dependents();
+    extern __shared__ int sm[];
+    int* hist = sm;                                  // [32 warps][kSchedBuckets]
+    int* scratch = hist + 32 * kSchedBuckets;        // 64
+    int* req_start = scratch + 64;                   // [B + 1] first item of each request
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per_item = p.rows_per_tile * kQTiles;
+    const int B = p.B;
+
+    // 1. per-request item counts, as a block-wide scan over contiguous chunks
+    const int chunk = (B + kSchedThreads - 1) / kSchedThreads;
+    const int b_begin = min(B, tid * chunk), b_end = min(B, b_begin + chunk);
+    int local = 0;
+    for (int b = b_begin; b < b_end; ++b) {
+        const RequestView r = load_request(p.cum_q, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size,
+                                           p.max_pages, p.num_tokens);
+        if (!r.ok)
+            atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
+        const int n = (r.ok && r.q_len > 0) ? p.Hkv * ((r.q_len + per_item - 1) / per_item) : 0;
+        req_start[b] = n;  // count for now
+        local += n;
+        if (p.debug) {
+            if (p.cum_kv != nullptr && r.ok && p.cum_kv[b + 1] - p.cum_kv[b] != r.kv_len)
+                atomicOr(p.err, (unsigned)B2PA_DEV_BAD_CUM_KV);
+            if (r.ok) {
+                const int pages = (r.kv_len + p.page_size - 1) / p.page_size;
+                for (int col = 0; col < pages; ++col) {
+                    const int id = p.block_tables[(long long)b * p.bt_stride + col];
+                    if (id < 0 || id >= p.num_pages)
+                        atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
+                }
+            }
+        }
+    }
+    int n_total = 0;
+    int run = block_exclusive_scan(local, scratch, &n_total);
+    for (int b = b_begin; b < b_end; ++b) {
+        const int n = req_start[b];
+        req_start[b] = run;
+        run += n;
+    }
+    if (tid == 0)
+        req_start[B] = n_total;
+    for (int k = tid; k < 32 * kSchedBuckets; k += kSchedThreads)
+        hist[k] = 0;
+    __syncthreads();
+    if (n_total > p.cap && tid == 0)
+        atomicOr(p.err, (unsigned)B2PA_DEV_OVERFLOW);
+
+    // item idx -> (b, kv head, it, bucket)
+    auto decode = [&](int idx, int4& item, int& bucket) {
+        int lo = 0, hi = B - 1;  // last b with req_start[b] <= idx
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (req_start[mid] <= idx)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int b = lo;
+        const int q_len = p.cum_q[b + 1] - p.cum_q[b];
+        const int kv_len = p.seq_lens[b];
+        const int n_it = (q_len + per_item - 1) / per_item;
+        const int loc = idx - req_start[b];
+        const int kvh = loc / n_it, it = loc % n_it;
+        const ItemGeom g = item_geometry(q_len, kv_len, it, p.rows_per_tile, p.window);
+        const int cost = (g.n_hi - g.n_lo + 1) * g.nq;
+        item = make_int4(b, kvh, it, cost);
+        bucket = min(cost, kCostCap);
+    };
+
+    const int seg = (n_total + 31) / 32;
+    const int s_begin = min(n_total, warp * seg), s_end = min(n_total, s_begin + seg);
+    int* my_hist = hist + warp * kSchedBuckets;
+
+    // 2. per-warp bucket counts
+    for (int base = s_begin; base < s_end; base += 32) {
+        const int idx = base + lane;
+        int4 item;
+        int bucket = -1;
+        if (idx < s_end)
+            decode(idx, item, bucket);
+        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
+        if (bucket >= 0 && lane == __ffs(grp) - 1)
+            my_hist[bucket] += __popc(grp);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // 3. offsets: buckets in descending order, warps in ascending order
+    int bucket_total = 0;
+    {
+        const int c = tid;  // kSchedBuckets == kSchedThreads
+        int acc = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int v = hist[w * kSchedBuckets + c];
+            hist[w * kSchedBuckets + c] = acc;
+            acc += v;
+        }
+        bucket_total = acc;
+    }
+    __syncthreads();
+    // exclusive scan over buckets from the top: thread t takes bucket kCostCap - t
+    int* tot = req_start + B + 1;  // [kSchedBuckets] scratch after req_start
+    tot[tid] = bucket_total;
+    __syncthreads();
+    const int mine = tot[kCostCap - tid];
+    __syncthreads();
+    const int start = block_exclusive_scan(mine, scratch, nullptr);
+    {
+        const int c = kCostCap - tid;
+        for (int w = 0; w < 32; ++w)
+            hist[w * kSchedBuckets + c] += start;
+    }
+    __syncthreads();
+
+    // 4. scatter
+    for (int base = s_begin; base < s_end; base += 32) {
+        const int idx = base + lane;
+        int4 item = make_int4(0, 0, 0, 0);
+        int bucket = -1;
+        if (idx < s_end)
+            decode(idx, item, bucket);
+        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
+        const unsigned lower = grp & ((1u << lane) - 1u);
+        if (bucket >= 0) {
+            const int pos = my_hist[bucket] + __popc(lower);
+            if (pos < p.cap)
+                p.items[pos] = item;
+        }
+        __syncwarp();
+        if (bucket >= 0 && lane == __ffs(grp) - 1)
+            my_hist[bucket] += __popc(grp);
+        __syncwarp();
+    }
+    if (tid == 0)
+        *p.count = n_total;
+}
+
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
+{
+    const size_t smem = sizeof(int) * ((size_t)32 * kSchedBuckets + 64 + (size_t)p.B + 1 + kSchedBuckets);
+    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    schedule_kernel<<<1, kSchedThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Debug gather: one CTA per (kv tile, kv head, request).  Warp 0 issues the
+// same per-page tensor-map loads as the attention producer into a
+// 128-row tile, then the CTA writes the rows below kv_len out contiguously,
+// undoing the 128-byte swizzle.
+// ---------------------------------------------------------------------------
+template <bool FP8>
+__global__ void __launch_bounds__(128) gather_kernel(const __grid_constant__ GatherParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* tile = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int D = p.D;
+    const int halves = FP8 ? 1 : D / 64;
+    const int half_bytes = kKvTile * 128;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(tile + halves * half_bytes);
+    const int j = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int kv_len = p.seq_lens[b];
+    if (kv_len < 0 || (long long)j * kKvTile >= kv_len)
+        return;
+    const int P = p.page_size;
+    if ((kv_len + P - 1) / P > p.max_pages) {
+        if (threadIdx.x == 0)
+            atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
+        return;
+    }
+    const long long row0 = p.cum_kv[b];
+    if (p.cum_kv[b + 1] - row0 != kv_len || row0 < 0 || row0 + kv_len > p.out_rows) {
+        if (threadIdx.x == 0)
+            atomicOr(p.err, (unsigned)B2PA_DEV_BAD_CUM_KV);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int rows = min(kKvTile, kv_len - j * kKvTile);
+    const int ppt = P >= kKvTile ? 1 : kKvTile / P;
+    const int box_rows = P >= kKvTile ? kKvTile : P;
+    for (int kind = 0; kind < 2; ++kind) {
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            const int first_col = (int)(((long long)j * kKvTile) / P);
+            const int slot0 = P > kKvTile ? (int)(((long long)j * kKvTile) % P) : 0;
+            const int col = first_col + lane;
+            const bool valid = lane < ppt && col < (kv_len + P - 1) / P;
+            const int page = valid ? p.block_tables[(long long)b * p.bt_stride + col] : 0;
+            if (valid && (page < 0 || page >= p.num_pages))
+                atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
+            const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar, nvalid * (uint32_t)box_rows * 128u * (uint32_t)halves);
+            __syncwarp();
+            if (valid) {
+                const uint32_t dst = smem_u32(tile) + (uint32_t)(lane * box_rows * 128);
+                for (int h = 0; h < halves; ++h)
+                    tma_load_4d(dst + h * half_bytes, kind ? &p.tm_v : &p.tm_k, bar, h * 64, slot0, kvh, page);
+            }
+        }
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(bar), kind)) {
+            if (clock64() - t0 > kWaitLimitCycles) {
+                if (threadIdx.x == 0)
+                    atomicOr(p.err, (unsigned)B2PA_DEV_TIMEOUT);
+                break;
+            }
+        }
+        uint8_t* out = kind ? p.v_out : p.k_out;
+        const int row_bytes = D * p.esize;       // bytes of one (token, head) row
+        const int chunks = row_bytes / 16;        // 16-byte chunks per row
+        for (int k = threadIdx.x; k < rows * chunks; k += blockDim.x) {
+            const int r = k / chunks, q = k % chunks;
+            const int h = q / 8, cq = q % 8;       // column block, chunk inside its 128-byte row
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + h * half_bytes + r * 128 + ((cq ^ (r & 7)) << 4));
+            const long long orow = (row0 + (long long)j * kKvTile + r) * p.Hkv + kvh;
+            *reinterpret_cast<uint4*>(out + orow * row_bytes + q * 16) = v;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaStream_t stream)
+{
+    const int tiles = (max_kv_len + kKvTile - 1) / kKvTile;
+    if (tiles == 0 || p.B == 0)
+        return cudaSuccess;
+    const int halves = fp8 ? 1 : p.D / 64;
+    const size_t smem = (size_t)halves * kKvTile * 128 + 64 + 1024;
+    auto kern = fp8 ? gather_kernel<true> : gather_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<dim3(tiles, p.Hkv, p.B), 128, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace b2pa

@@ -1,0 +1,335 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bars (fixed by the benchmark spec for bf16 outputs on N(0,1) inputs):
+max-abs <= 2e-2 and mean-abs <= 2e-3; FP8 KV: max-abs <= 3e-2 against the
+oracle fed the same e4m3 values and scales.  Integer work (gathered K/V and
+the work list) must match bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workload
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN, TOL_MAX_FP8 = 2e-2, 2e-3, 3e-2
+DEV = "cuda:0"
+
+
+def _to_dev(inp):
+    d = {}
+    for name in ("q", "k_pool", "v_pool", "block_tables", "seq_lens", "cum_q", "cum_kv"):
+        d[name] = getattr(inp, name).to(DEV)
+    d["sinks"] = None if inp.sinks is None else inp.sinks.to(DEV)
+    return d
+
+
+def _run(b2pa, inp, path="auto", out=None, dev=None):
+    b2pa.set_kernel_path(path)
+    try:
+        d = dev or _to_dev(inp)
+        if out is None:
+            out = torch.full_like(d["q"], float("nan"))
+        b2pa.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], inp.max_q_len,
+                               inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"], d["cum_kv"],
+                               inp.window_left, out, inp.layout, d["sinks"])
+        bits = b2pa.device_status()
+    finally:
+        b2pa.set_kernel_path("auto")
+    return out, bits
+
+
+def _compare(got, inp, rows=None, fp8=None):
+    """got: [T, H, D] device tensor.  rows: None = all, else int64 token*H+h."""
+    fp8 = inp.meta.get("kv_dtype") == "fp8_e4m3" if fp8 is None else fp8
+    ref, st, _ = oracle.attention(inp, rows=rows)
+    assert (st == 0).all()
+    T, H, D = got.shape
+    g = got.float().cpu().reshape(T * H, D).double()
+    if rows is not None:
+        g = g[torch.as_tensor(rows)]
+    err = (g - torch.from_numpy(ref)).abs()
+    assert torch.isfinite(g).all(), "non-finite output"
+    mx, mean = err.max().item(), err.mean().item()
+    if fp8:
+        assert mx <= TOL_MAX_FP8, (mx, mean)
+    else:
+        assert mx <= TOL_MAX and mean <= TOL_MEAN, (mx, mean)
+    return mx, mean
+
+
+# ----------------------------------------------------------------- tensor-core path, small cases
+
+TC_CASES = [
+    # (q_lens, kv_lens, H, Hkv, D, P, layout, window, sinks, kv_dtype)
+    ([70, 130, 5], [300, 130, 5], 8, 2, 128, 32, "HND", -1, True, "bf16"),
+    ([64, 1, 200], [64, 513, 700], 32, 8, 128, 16, "NHD", -1, False, "bf16"),
+    ([257, 33], [257, 33], 4, 4, 128, 64, "HND", -1, False, "bf16"),          # MHA, G = 1
+    ([150, 90], [900, 90], 64, 8, 128, 128, "NHD", -1, True, "bf16"),          # G = 8
+    ([300], [1200], 16, 1, 128, 256, "HND", -1, False, "bf16"),               # G = 16, P > tile
+    ([200, 77], [200, 300], 16, 2, 64, 16, "HND", 127, True, "bf16"),          # D = 64, window
+    ([129, 3, 260], [129, 500, 260], 8, 2, 64, 8, "NHD", -1, False, "bf16"),
+    ([100, 140], [1000, 140], 8, 2, 128, 32, "HND", 0, True, "bf16"),          # window 0
+    ([333, 50], [700, 50], 8, 2, 128, 32, "HND", 200, False, "bf16"),
+    ([96, 1, 40], [4000, 3000, 40], 32, 8, 128, 32, "HND", -1, False, "fp8_e4m3"),
+    ([300, 7], [300, 600], 8, 2, 128, 64, "NHD", 77, True, "fp8_e4m3"),
+    ([0, 40, 0, 10], [10, 100, 0, 10], 8, 2, 128, 32, "HND", -1, False, "bf16"),  # empty requests
+    ([24, 24], [24, 24], 12, 4, 128, 32, "HND", -1, True, "bf16"),              # G = 3: rows 126 of 128
+]
+
+
+@pytest.mark.parametrize("case", range(len(TC_CASES)))
+def test_tcgen05_parity_small(cuda_lib, case):
+    ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = TC_CASES[case]
+    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=100 + case,
+                         table_pad="garbage")
+    assert cuda_lib.query_path(inp.q.to(DEV), (inp.k_pool.to(DEV), inp.v_pool.to(DEV)), kv_layout=lay) == "tcgen05"
+    out, bits = _run(cuda_lib, inp, "tcgen05")
+    assert bits == 0
+    _compare(out, inp)
+
+
+@pytest.mark.parametrize("case", range(len(TC_CASES)))
+def test_generic_parity_small(cuda_lib, case):
+    ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = TC_CASES[case]
+    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=100 + case)
+    out, bits = _run(cuda_lib, inp, "generic")
+    assert bits == 0
+    _compare(out, inp)
+
+
+GENERIC_ONLY = [
+    ([5, 3], [9, 3], 2, 1, 16, 4, "HND", -1, False, "bf16"),
+    ([17, 9], [40, 9], 6, 3, 40, 5, "NHD", 6, True, "bf16"),
+    ([33], [33], 4, 2, 256, 7, "HND", -1, True, "fp8_e4m3"),
+    ([12, 1], [12, 30], 3, 1, 96, 3, "NHD", -1, False, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(GENERIC_ONLY)))
+def test_generic_only_shapes(cuda_lib, case):
+    ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = GENERIC_ONLY[case]
+    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=300 + case)
+    assert cuda_lib.query_path(inp.q.to(DEV), (inp.k_pool.to(DEV), inp.v_pool.to(DEV)), kv_layout=lay) == "generic"
+    out, bits = _run(cuda_lib, inp)
+    assert bits == 0
+    _compare(out, inp)
+
+
+def test_tiny_config(cuda_lib):
+    inp = workload.config(1)
+    out, bits = _run(cuda_lib, inp)
+    assert bits == 0
+    _compare(out, inp)
+
+
+# ----------------------------------------------------------------- the named workloads at full size
+
+def _sample_rows(inp, n_random, seed):
+    """Boundary rows of every request (first / last query, window edge) plus random rows."""
+    H = inp.num_heads
+    g = np.random.default_rng(seed)
+    rows = set()
+    for b in range(inp.batch):
+        q0, q1 = int(inp.cum_q[b]), int(inp.cum_q[b + 1])
+        if q1 == q0:
+            continue
+        toks = {q0, q1 - 1, min(q1 - 1, q0 + 1)}
+        if inp.window_left >= 0:
+            toks.add(min(q1 - 1, q0 + inp.window_left))
+        for t in toks:
+            for h in (0, H - 1, int(g.integers(H))):
+                rows.add(t * H + h)
+    T = inp.q.shape[0]
+    rows.update(g.integers(0, T * H, size=n_random).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("index,window", [(2, None), (3, None), (4, None), (4, -1), (5, None)])
+def test_named_workloads_sampled(cuda_lib, index, window):
+    inp = workload.config(index, window_left=window)
+    out, bits = _run(cuda_lib, inp)
+    assert bits == 0
+    rows = _sample_rows(inp, 600, seed=index)
+    _compare(out, inp, rows=rows)
+    # properties that hold at any size: finite everywhere, and every row of a
+    # valid request was written (the NaN fill is gone)
+    assert torch.isfinite(out).all()
+
+
+# ----------------------------------------------------------------- bit-exact integer work
+
+@pytest.mark.parametrize("layout,kvd,P,D", [("HND", "bf16", 32, 128), ("NHD", "bf16", 16, 64),
+                                            ("HND", "fp8_e4m3", 32, 128), ("NHD", "bf16", 256, 128),
+                                            ("HND", "bf16", 8, 64)])
+def test_debug_gather_bit_exact(cuda_lib, layout, kvd, P, D):
+    inp = workload.build([10, 1, 300], [130, 77, 600], 8, 4, D, P, layout, kv_dtype=kvd, seed=7, table_pad="garbage")
+    d = _to_dev(inp)
+    total = int(inp.seq_lens.sum())
+    k_out, v_out = cuda_lib.debug_gather((d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], d["cum_kv"],
+                                         total, layout)
+    assert cuda_lib.device_status() == 0
+    k_ref, ok1 = oracle.gather(inp, "k")
+    v_ref, ok2 = oracle.gather(inp, "v")
+    assert ok1 and ok2
+    assert torch.equal(k_out.cpu().view(torch.uint8), k_ref.view(torch.uint8))
+    assert torch.equal(v_out.cpu().view(torch.uint8), v_ref.view(torch.uint8))
+
+
+def test_debug_gather_strided_views(cuda_lib):
+    # one [N, 2, P, Hkv, D] cache viewed as HND pools with NHD strides
+    # (TokenSpeed _get_kv_cache_permuted), Hkv = 1 (canonicalize_stride's case)
+    inp = workload.build([5, 40], [200, 40], 4, 1, 128, 32, "NHD", seed=8, combined_kv=True)
+    hnd = workload.build([5, 40], [200, 40], 4, 1, 128, 32, "NHD", seed=8, combined_kv=True)
+    hnd.layout = "HND"
+    hnd.k_pool = inp.k_pool.permute(0, 2, 1, 3)
+    hnd.v_pool = inp.v_pool.permute(0, 2, 1, 3)
+    d = _to_dev(hnd)
+    total = int(inp.seq_lens.sum())
+    k_out, v_out = cuda_lib.debug_gather((d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], d["cum_kv"],
+                                         total, "HND")
+    k_ref, _ = oracle.gather(inp, "k")
+    v_ref, _ = oracle.gather(inp, "v")
+    assert torch.equal(k_out.cpu().view(torch.uint8), k_ref.view(torch.uint8))
+    assert torch.equal(v_out.cpu().view(torch.uint8), v_ref.view(torch.uint8))
+    out, bits = _run(cuda_lib, hnd, "tcgen05")
+    assert bits == 0
+    _compare(out, inp)
+
+
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5])
+def test_worklist_bit_exact(cuda_lib, index):
+    inp = workload.config(index)
+    d = _to_dev(inp)
+    items, geo = cuda_lib.debug_worklist(d["q"], d["k_pool"], d["block_tables"], d["seq_lens"], d["cum_q"],
+                                         inp.max_q_len, inp.max_kv_len, inp.window_left, inp.layout)
+    ref = oracle.worklist(inp, geo["rows_per_tile"], geo["n_qtiles"], geo["kv_tile"], geo["cost_cap"])
+    assert items.shape == ref.shape
+    assert np.array_equal(items, ref)
+
+
+@pytest.mark.parametrize("window", [-1, 0, 5, 300])
+def test_worklist_bit_exact_ragged(cuda_lib, window):
+    ql = [1, 0, 700, 64, 65, 3000, 31]
+    kl = [1, 5, 900, 64, 1000, 3000, 4000]
+    inp = workload.build(ql, kl, 16, 2, 128, 32, "HND", window_left=window, seed=9)
+    d = _to_dev(inp)
+    items, geo = cuda_lib.debug_worklist(d["q"], d["k_pool"], d["block_tables"], d["seq_lens"], d["cum_q"],
+                                         inp.max_q_len, inp.max_kv_len, window, "HND")
+    ref = oracle.worklist(inp, geo["rows_per_tile"], geo["n_qtiles"], geo["kv_tile"], geo["cost_cap"])
+    assert np.array_equal(items, ref)
+
+
+# ----------------------------------------------------------------- robustness
+
+@pytest.mark.parametrize("path", ["tcgen05", "generic"])
+def test_poisoned_pool_tails_and_padding(cuda_lib, path):
+    inp = workload.build([70, 9, 130], [301, 9, 200], 8, 2, 128, 32, "HND", with_sinks=True, seed=11,
+                         table_pad="garbage", pool_factor=2.0)
+    # NaN into every slot no request reads at a position below its kv_len
+    used = set()
+    for b in range(inp.batch):
+        for t in range(int(inp.seq_lens[b])):
+            used.add((int(inp.block_tables[b, t // 32]), t % 32))
+    for pg in range(inp.k_pool.shape[0]):
+        for sl in range(32):
+            if (pg, sl) not in used:
+                inp.k_pool[pg, :, sl] = float("nan")
+                inp.v_pool[pg, :, sl] = float("nan")
+    out, bits = _run(cuda_lib, inp, path)
+    assert bits == 0
+    _compare(out, inp)
+
+
+def test_poisoned_fp8_tails(cuda_lib):
+    inp = workload.build([40, 100], [77, 300], 8, 2, 128, 32, "HND", kv_dtype="fp8_e4m3", seed=12)
+    nan8 = torch.tensor([0x7F], dtype=torch.uint8).view(torch.float8_e4m3fn)
+    used = set()
+    for b in range(inp.batch):
+        for t in range(int(inp.seq_lens[b])):
+            used.add((int(inp.block_tables[b, t // 32]), t % 32))
+    for pg in range(inp.k_pool.shape[0]):
+        for sl in range(32):
+            if (pg, sl) not in used:
+                inp.k_pool[pg, :, sl] = nan8
+                inp.v_pool[pg, :, sl] = nan8
+    out, bits = _run(cuda_lib, inp, "tcgen05")
+    assert bits == 0
+    _compare(out, inp)
+
+
+@pytest.mark.parametrize("path", ["tcgen05", "generic"])
+def test_output_canaries_and_bad_request(cuda_lib, path):
+    inp = workload.build([30, 20, 25], [60, 20, 25], 8, 2, 128, 32, "HND", seed=13)
+    d = _to_dev(inp)
+    # request 1 claims 20 queries but only 10 keys: rejected, its rows untouched
+    d["seq_lens"][1] = 10
+    T, H, D = inp.q.shape
+    big = torch.full((T + 8, H, D), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = big[4:4 + T]
+    cuda_lib.set_kernel_path(path)
+    try:
+        cuda_lib.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                   inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"], None,
+                                   -1, out, "HND")
+        bits = cuda_lib.device_status()
+    finally:
+        cuda_lib.set_kernel_path("auto")
+    assert bits & cuda_lib.DEV_BAD_REQUEST
+    assert (big[:4] == 7).all() and (big[4 + T:] == 7).all()
+    assert (out[30:50] == 7).all()
+    ok = inp.cum_q.tolist()
+    rows = np.array([t * H + h for t in list(range(0, 30)) + list(range(50, 75)) for h in range(H)])
+    _compare(out, inp, rows=rows)
+
+
+def test_bad_page_id_flagged(cuda_lib):
+    inp = workload.build([16], [100], 8, 2, 128, 32, "HND", seed=14)
+    d = _to_dev(inp)
+    d["block_tables"][0, 1] = inp.k_pool.shape[0] + 10
+    cuda_lib.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], 16, 100,
+                               inp.bmm1_scale, 1.0, d["cum_q"], None, -1, None, "HND")
+    assert cuda_lib.device_status() & cuda_lib.DEV_BAD_PAGE
+
+
+def test_bitwise_deterministic(cuda_lib):
+    inp = workload.config(2)
+    d = _to_dev(inp)
+    a, _ = _run(cuda_lib, inp, dev=d)
+    b, _ = _run(cuda_lib, inp, dev=d)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_cuda_graph_replay(cuda_lib):
+    inp = workload.build([100, 260], [400, 260], 8, 2, 128, 32, "HND", seed=15, with_sinks=True)
+    d = _to_dev(inp)
+    s = torch.cuda.Stream()
+    out = torch.zeros_like(d["q"])
+    with torch.cuda.stream(s):
+        args = (d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], inp.max_q_len, inp.max_kv_len,
+                inp.bmm1_scale, inp.bmm2_scale, d["cum_q"], d["cum_kv"], -1, out, "HND", d["sinks"])
+        cuda_lib.context_attention(*args, stream=s)  # sizes this stream's workspace
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            cuda_lib.context_attention(*args, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    _compare(out, inp)
+
+
+def test_invalid_arguments_rejected_on_host(cuda_lib):
+    inp = workload.build([4], [8], 4, 2, 128, 32, "HND", seed=16)
+    d = _to_dev(inp)
+    with pytest.raises(cuda_lib.B2paError):
+        cuda_lib.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], 4, 8,
+                                   -1.0, 1.0, d["cum_q"], None, -1, None, "HND")
+    with pytest.raises(cuda_lib.B2paError):
+        q3 = d["q"][:, :3]
+        cuda_lib.context_attention(q3, (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], 4, 8, 0.1,
+                                   1.0, d["cum_q"], None, -1, None, "HND")
