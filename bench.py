@@ -1,0 +1,515 @@
+#!/usr/bin/env python
+"""Benchmark of batched paged-KV context attention on GB300.
+
+Workload: the Llama-3-8B-shaped prefill (batch 8, q_len = kv_len ~ U[512, 2048],
+32 query heads / 8 kv heads, head_dim 128, page_size 32, HND, bf16 N(0,1),
+pages scattered over a pool twice the needed size, causal), drawn by
+workload.config(2) with seed 1236.
+
+Metric: effective causal TFLOP/s = 4 * head_dim * num_heads * (visible (query,
+key) pairs) / time, with the fraction of the measured dense-bf16 tensor peak.
+
+One "step" = one b2pa_context_attention call over the whole batch (scheduler
++ attention kernel).  Inputs are resident in HBM; L2 is flushed (a 512 MiB
+write) before every timed step, outside the timed events.  Prints one JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded row
+sample of the same workload (there is no other reference implementation).
+Under torchrun with N > 1 every rank runs its own replica (no collective on
+the data path); value = all ranks' work / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload  # noqa: E402
+
+METRIC = "effective causal TFLOPS of paged prefill attention and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD_INDEX = 2
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tc_llama3_8b_prefill_traffic.json")
+KERNEL_SOURCES = ["attn_tc.cu", "common.cuh", "ptx.cuh"]
+
+
+# --------------------------------------------------------------------------- workload arithmetic
+
+def visible_pairs(inp) -> int:
+    """Sum over requests and queries of the number of visible keys (per head)."""
+    total = 0
+    W = inp.window_left
+    for ql, kl in zip(inp.q_lens, inp.kv_lens):
+        if ql <= 0:
+            continue
+        pos = np.arange(kl - ql, kl, dtype=np.int64)
+        vis = pos + 1 if W < 0 else np.minimum(pos + 1, W + 1)
+        total += int(vis.sum())
+    return total
+
+
+def step_flops(inp) -> float:
+    return 4.0 * inp.head_dim * inp.num_heads * visible_pairs(inp)
+
+
+def workload_config(inp, l2: str) -> dict:
+    return {
+        "workload": inp.name,
+        "batch": inp.batch,
+        "num_tokens": int(inp.q.shape[0]),
+        "num_heads": inp.num_heads,
+        "num_kv_heads": inp.num_kv_heads,
+        "head_dim": inp.head_dim,
+        "page_size": inp.page_size,
+        "kv_layout": inp.layout,
+        "kv_dtype": inp.meta.get("kv_dtype"),
+        "seed": inp.seed,
+        "visible_pairs_per_head": visible_pairs(inp),
+        "l2": l2,
+        "parallelism": "replicas",
+    }
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["bf16_tflops"]), float(p.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_kv_prefill_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    t = json.load(open(TRAFFIC_FILE))
+    if t.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        load = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in load if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons,
+            "samples": len(rows),
+            "samples_under_load": len(load),
+            "power_w_max": max((num(r[3]) or 0) for r in rows) if rows else None,
+        }
+
+
+# --------------------------------------------------------------------------- distributed helpers
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_rows(inp, fraction: float, seed: int) -> np.ndarray:
+    T, H = inp.q.shape[0], inp.num_heads
+    n = max(1, int(T * H * fraction))
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(T * H, size=n, replace=False)).astype(np.int64)
+
+
+def rows_pairs(inp, rows: np.ndarray) -> int:
+    H = inp.num_heads
+    cq = inp.cum_q.numpy().astype(np.int64)
+    kv = inp.seq_lens.numpy().astype(np.int64)
+    tok = rows // H
+    b = np.searchsorted(cq, tok, side="right") - 1
+    i = tok - cq[b]
+    pos = kv[b] - (cq[b + 1] - cq[b]) + i
+    W = inp.window_left
+    vis = pos + 1 if W < 0 else np.minimum(pos + 1, W + 1)
+    return int(vis.sum())
+
+
+def time_oracle(inp, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    _, st, threads = oracle.attention(inp, rows=rows)
+    dt = time.perf_counter() - t0
+    assert (st == 0).all()
+    flops = 4.0 * inp.head_dim * rows_pairs(inp, rows)
+    return flops, dt, threads
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import paged_kv_prefill_gb300 as b2pa
+    from paged_kv_prefill_gb300 import build as b2pa_build
+
+    if rank == 0 or world == 1:
+        b2pa_build.build()
+    barrier(world)
+    b2pa.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workload.config(WORKLOAD_INDEX)
+    flops = step_flops(inp)
+    q = inp.q.to(dev)
+    k = inp.k_pool.to(dev)
+    v = inp.v_pool.to(dev)
+    bt = inp.block_tables.to(dev)
+    sl = inp.seq_lens.to(dev)
+    cq = inp.cum_q.to(dev)
+    ck = inp.cum_kv.to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(qq=q, oo=out):
+        b2pa.context_attention(qq, (k, v), bt, sl, inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale,
+                               cq, ck, inp.window_left, oo, inp.layout, None, stream=stream)
+
+    assert b2pa.query_path(q, (k, v), out, inp.layout) == "tcgen05"
+    if args.profile:
+        # for ncu: W warm-up calls then K calls, nothing else (no numbers are reported)
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i)
+            call()
+        torch.cuda.synchronize()
+        print(f"profile run: {args.warmup} + {args.steps} calls, device bits {b2pa.device_status()}", flush=True)
+        return
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler.start()
+    # bring the clocks up (not timed), then warm up
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    bits = b2pa.device_status()
+    if bits:
+        raise RuntimeError(f"device error bits {bits} during warm-up")
+
+    # ---- timed region: K steps, each bracketed by events; L2 flushed outside the events
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i)
+        ev0[i].record(stream)
+        call()
+        ev1[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = sum(step_ms)
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    all_flops = sum_over_ranks(flops * K, world, dev)
+    value = all_flops / (total_ms_max * 1e-3) / 1e12
+
+    # ---- the attention kernel alone: events recorded by the library around its launch
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ka + kb:
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i)
+        b2pa.set_timing_events(ka[i], kb[i])
+        call()
+    b2pa.set_timing_events(None, None)
+    torch.cuda.synchronize()
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ka, kb))
+    bits = b2pa.device_status()
+    if bits:
+        raise RuntimeError(f"device error bits {bits} during the timed region")
+
+    # ---- end to end through the public call with host buffers: H2D inputs, call, D2H result
+    host = {n: getattr(inp, n).pin_memory() for n in ("q", "k_pool", "v_pool", "block_tables", "seq_lens", "cum_q",
+                                                       "cum_kv")}
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    Ke = max(3, min(K, 50))
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(Ke)]
+
+    def e2e_step(i=None):
+        if i is not None:
+            e0[i].record(stream)
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        b2pa.context_attention(dbuf["q"], (dbuf["k_pool"], dbuf["v_pool"]), dbuf["block_tables"], dbuf["seq_lens"],
+                               inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, dbuf["cum_q"],
+                               dbuf["cum_kv"], inp.window_left, out, inp.layout, None, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+        if i is not None:
+            e1[i].record(stream)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    for i in range(Ke):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)), world, dev)
+    e2e_value = sum_over_ranks(flops * Ke, world, dev) / (e2e_ms * 1e-3) / 1e12
+
+    peak_tf, hbm_gbs, peak_src = peaks()
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    traffic = recorded_traffic()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = oracle_rows(inp, args.cpu_fraction, seed=1)
+        f, dt, threads = time_oracle(inp, rows)
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(rows)} of {inp.q.shape[0] * inp.num_heads} (token, head) rows "
+                         f"({args.cpu_fraction:.3f} of the batch, seeded), fp64, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": total_ms_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": workload_config(inp, "flushed: 512 MiB write before every timed step, outside the events"),
+            "fraction_of_peak": value / peak_tf,
+            "roofline": {
+                "bound": "tensor",
+                "achieved": achieved,
+                "peak": peak_tf,
+                "unit": UNIT,
+                "frac": achieved / peak_tf,
+                "traffic": traffic,
+                "peak_source": f"{peak_src} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "kernel": "attention_tc_kernel<128,false>",
+                "kernel_ms": kern_ms,
+                "flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": algorithmic_bytes(inp),
+                "achieved_hbm_gbs": algorithmic_bytes(inp) / (kern_ms * 1e-3) / 1e9,
+                "hbm_peak_gbs": hbm_gbs,
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": Ke},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def algorithmic_bytes(inp) -> int:
+    """Bytes one launch must move at least: Q and O once, each used K/V token once per kv head."""
+    T, H, D = inp.q.shape
+    qo = 2 * T * H * D * 2
+    kv_tok = sum(inp.kv_lens)
+    es = 1 if inp.meta.get("kv_dtype") == "fp8_e4m3" else 2
+    kv = 2 * kv_tok * inp.num_kv_heads * D * es
+    tables = inp.block_tables.numel() * 4 + (inp.batch * 3 + 2) * 4
+    return qo + kv + tables
+
+
+# --------------------------------------------------------------------------- reference arm (the CPU oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    inp = workload.config(WORKLOAD_INDEX)
+    # size each step so that warm-up + timed steps take about two minutes
+    probe = oracle_rows(inp, 0.01, seed=2)
+    f, dt, threads = time_oracle(inp, probe)
+    rate = f / dt
+    steps = args.steps + args.warmup
+    budget = min(10.0, 120.0 / max(1, steps))
+    fraction = min(1.0, budget * rate / step_flops(inp))
+    for i in range(args.warmup):
+        time_oracle(inp, oracle_rows(inp, fraction, seed=100 + i))
+    tot_f = tot_t = 0.0
+    for i in range(args.steps):
+        f, dt, threads = time_oracle(inp, oracle_rows(inp, fraction, seed=1000 + i))
+        tot_f += f
+        tot_t += dt
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: {fraction:.4f} of the batch's (token, head) rows, seeded, fp64 CPU oracle, "
+              f"{tot_t / args.steps:.2f} s per step")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(inp, "n/a (host CPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-fraction", type=float, default=0.125)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="only W + K calls of the workload (for ncu); prints no measurement")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -192,6 +192,13 @@ B2PA_API int b2pa_query_path(const b2pa_tensor* q, const b2pa_tensor* k_pool, co
  * cum_kv against seq_lens.  Off by default. */
 B2PA_API int b2pa_set_debug_checks(int32_t on);
 
+/* Instrumentation (no counterpart on the pages): when both are non-NULL, later
+ * b2pa_context_attention calls on the tensor-core path record start_event just
+ * before and stop_event just after launching the attention kernel, on the call's
+ * stream, so a caller can time that kernel alone.  The arguments are cudaEvent_t
+ * handles owned by the caller; NULL, NULL turns recording off. */
+B2PA_API int b2pa_set_timing_events(void* start_event, void* stop_event);
+
 /* Human-readable name of a b2pa_status. */
 B2PA_API const char* b2pa_status_string(int32_t status);
 

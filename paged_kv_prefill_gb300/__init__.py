@@ -45,6 +45,7 @@ EXPORTED = [
     "b2pa_set_kernel_path",
     "b2pa_query_path",
     "b2pa_set_debug_checks",
+    "b2pa_set_timing_events",
     "b2pa_status_string",
     "b2pa_last_error_message",
     "b2pa_release",
@@ -94,6 +95,8 @@ def load(path: str = LIB_PATH):
     lib.b2pa_set_kernel_path.restype = ctypes.c_int
     lib.b2pa_query_path.argtypes = [P, P, P, P, ctypes.c_int32]
     lib.b2pa_query_path.restype = ctypes.c_int
+    lib.b2pa_set_timing_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.b2pa_set_timing_events.restype = ctypes.c_int
     lib.b2pa_set_debug_checks.argtypes = [ctypes.c_int32]
     lib.b2pa_set_debug_checks.restype = ctypes.c_int
     lib.b2pa_status_string.argtypes = [ctypes.c_int32]
@@ -256,6 +259,15 @@ def query_path(query, kv_cache, out=None, kv_layout="HND") -> str:
 
 def set_debug_checks(on: bool):
     load().b2pa_set_debug_checks(1 if on else 0)
+
+
+def set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    """Record start/stop around each later attention-kernel launch (tensor-core path); None, None turns it off."""
+    lib = load()
+    if start is None or stop is None:
+        lib.b2pa_set_timing_events(None, None)
+    else:
+        lib.b2pa_set_timing_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
 
 
 def release():

@@ -6,18 +6,22 @@
 // rule of the TokenSpeed trtllm backend (_init_extend_metadata); see the
 // header of include/b2pa.h.  The design below is ours.
 //
-// One CTA per SM loops over the scheduler's work list.  A work item is (request
-// b, kv head, item index): two query tiles of 128 MMA rows each, a row being
-// one (token, query head) pair of the kv head's group (rows_per_tile tokens x
-// G heads).  Both query tiles stream the same K/V tiles of 128 keys.
+// One CTA per SM.  Work items come from the scheduler's longest-first list;
+// the producer warp takes the next one with an atomic counter and hands its
+// index to the other roles through a small shared-memory ring.  A work item
+// is (request b, kv head, item index): two query tiles of 128 MMA rows, a row
+// being one (token, query head) pair of the kv head's group (rows_per_tile
+// tokens x G heads).  Both query tiles stream the same K/V tiles of 128 keys.
 //
-//   warp 0        producer: TMA loads of Q (3-D map) and of K/V pages (4-D
-//                 map, one box per page and 128-byte column block), through
-//                 a ring of shared-memory stages with full/empty mbarriers.
+//   warp 0        producer: item fetch; TMA loads of Q (3-D map, double
+//                 buffered across items where shared memory allows) and of
+//                 K/V pages (4-D map, one box per page and 128-byte column
+//                 block) through a ring of stages with full/empty mbarriers.
 //   warp 1        MMA issuer (one lane): S_t = Q_t K^T into TMEM, then
-//                 O_t += P_t V with P_t read from TMEM, for t = 0, 1,
-//                 interleaved so the tensor core works on one tile while
-//                 the other tile's softmax runs.  Owns the TMEM allocation.
+//                 O_t += P_t V with P_t read from TMEM, for t = 0, 1, in the
+//                 order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) so the tensor
+//                 core works on one tile while the other tile's softmax runs.
+//                 Owns the TMEM allocation.
 //   warps 4-7     softmax of query tile 0 (one thread per row), O rescale,
 //                 and the epilogue (bmm2_scale / denominator, bf16 stores).
 //   warps 8-11    the same for query tile 1.
@@ -25,7 +29,9 @@
 //                 layout, and the Q tile from bf16 to f16.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
-// P_t (16-bit, two per column) overwrites the first 64 columns of S_t.
+// P_t (16-bit, two per column) overwrites the first 64 columns of S_t; it is
+// handed to the MMA warp in two halves (keys 0-63, 64-127) so that P V on the
+// first half overlaps the softmax of the second.
 //
 // Every wait is bounded: after kWaitLimitCycles the CTA raises
 // B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies and
@@ -41,36 +47,44 @@ struct TcCfg {
     static constexpr int kHalfBytes = kQRows * 128;   // one column block of a 128-row tile
     static constexpr int kQTileBytes = kHalves * kHalfBytes;
     static constexpr int kKvTileBytes = kHalves * kHalfBytes;
-    static constexpr int kStages = D == 128 ? (FP8 ? 3 : 4) : 8;
-    static constexpr int kF8Stages = FP8 ? 3 : 0;
+    // A kv tile j is in use from S(j) to PV(j); the ring must also hold the
+    // next K and V in flight: at least 4 stages, 5 where shared memory allows.
+    static constexpr int kQBufs = D == 128 ? 1 : 2;                 // Q buffers (items in flight)
+    static constexpr int kStages = D == 128 ? (FP8 ? 4 : 5) : 8;    // 16-bit K/V ring
+    static constexpr int kF8Stages = FP8 ? 2 : 0;                   // e4m3 staging ring
     static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
     static constexpr int kThreads = FP8 ? 512 : 384;
+    static constexpr int kItemSlots = 4;
+    static constexpr int kItemConsumerWarps = 1 + 8 + (FP8 ? 4 : 0);
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 2 * kKvTile;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffRing = kOffQ + kQTiles * kQTileBytes;
+    static constexpr int kOffRing = kOffQ + kQBufs * kQTiles * kQTileBytes;
     static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
     static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 + 3 * kQTiles + 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 * kQBufs + 4 * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "fp8 path is D = 128");
     static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
+    static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct Bars {
-    uint64_t* full;
-    uint64_t* empty;
-    uint64_t* f8full;
-    uint64_t* f8empty;
-    uint64_t* q_full;
-    uint64_t* q_empty;
-    uint64_t* q_conv;
-    uint64_t* s_full;
-    uint64_t* p_full;
-    uint64_t* o_full;
+    uint64_t* full;      // [kStages]  16-bit K/V tile landed (TMA bytes, or converter warps)
+    uint64_t* empty;     // [kStages]  tile consumed by the MMAs
+    uint64_t* f8full;    // [kF8Stages]
+    uint64_t* f8empty;   // [kF8Stages]
+    uint64_t* q_full;    // [kQBufs]   Q tiles landed
+    uint64_t* q_empty;   // [kQBufs]   last Q K^T of the item done
+    uint64_t* q_conv;    // [kQBufs]   (FP8) Q converted to f16
+    uint64_t* s_full;    // [2]        S_t in TMEM
+    uint64_t* p_full;    // [2][2]     half h of P_t in TMEM (4 softmax warps)
+    uint64_t* o_full;    // [2]        last P V of the item done
     uint64_t* drain;
+    uint64_t* it_full;   // [kItemSlots] item index posted
+    uint64_t* it_empty;  // [kItemSlots] item index read by every consumer warp
 };
 
 struct Ctx {
@@ -78,6 +92,7 @@ struct Ctx {
     Bars bar;
     uint32_t tmem;
     int n_items;
+    volatile int* item_slot;
     volatile int* abort_flag;
 };
 
@@ -130,9 +145,25 @@ __device__ __forceinline__ ItemInfo read_item(const AttnParams& p, int w)
     return r;
 }
 
+// The n-th item index of this CTA (-1: no more work), as posted by the producer.
+template <int kSlots>
+__device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint32_t n, bool* ok)
+{
+    const uint32_t s = n % kSlots;
+    if (!wait_bar(&c.bar.it_full[s], (n / kSlots) & 1, c.abort_flag, p.err)) {
+        *ok = false;
+        return -1;
+    }
+    const int w = c.item_slot[s];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(&c.bar.it_empty[s]);
+    return w;
+}
+
 // ---------------------------------------------------------------------------
-// Producer: warp 0.  Lane l loads page l of a kv tile (one TMA box per
-// 128-byte column block); lane 0 posts the byte count first.
+// Producer: warp 0.  Lane 0 takes items; lane l loads page l of a kv tile (one
+// TMA box per 128-byte column block) after lane 0 posted the byte count.
 // ---------------------------------------------------------------------------
 template <int D, bool FP8>
 __device__ void producer_role(const AttnParams& p, const Ctx& c)
@@ -152,22 +183,35 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     const uint32_t q_box_bytes = (uint32_t)(p.G * p.rows_per_tile * 128);
 
     uint32_t ring_idx = 0;
-    int item_iter = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
-        const ItemInfo it = read_item(p, w);
-        // Q tiles of this item (after the previous item's last Q K^T has read the buffer)
-        if (item_iter > 0 && !wait_bar(c.bar.q_empty, (item_iter - 1) & 1, c.abort_flag, p.err)) {
-            ok = false;
+    for (uint32_t n = 0; ok; ++n) {
+        // post the next item index
+        const uint32_t slot = n % C::kItemSlots;
+        if (!wait_bar(&c.bar.it_empty[slot], ((n / C::kItemSlots) & 1) ^ 1, c.abort_flag, p.err))
             break;
+        int w = 0;
+        if (lane == 0) {
+            w = atomicAdd(p.counter, 1);
+            if (w >= c.n_items)
+                w = -1;
+            c.item_slot[slot] = w;
+            mbar_arrive(&c.bar.it_full[slot]);
         }
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (w < 0)
+            break;
+        const ItemInfo it = read_item(p, w);
+        // Q tiles, into the buffer of this item once its previous user is done
+        const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
+        if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c.abort_flag, p.err))
+            break;
         if (lane == 0)
-            mbar_arrive_expect_tx(c.bar.q_full, (uint32_t)(it.g.nq * C::kHalves) * q_box_bytes);
+            mbar_arrive_expect_tx(&c.bar.q_full[qb], (uint32_t)(it.g.nq * C::kHalves) * q_box_bytes);
         __syncwarp();
         if (lane < it.g.nq * C::kHalves) {
             const int t = lane / C::kHalves, h = lane % C::kHalves;
-            tma_load_3d(q_smem + t * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, c.bar.q_full, h * 64,
-                        it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
+            tma_load_3d(q_smem + (qb * kQTiles + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
+                        h * 64, it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
         }
         const int* bt_row = p.block_tables + (long long)it.b * p.bt_stride;
         const int n_pages_valid = (it.kv_len + P - 1) / P;
@@ -222,31 +266,42 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                                  ((uint32_t)(kQRows >> 4) << 24);
     constexpr uint32_t kIdescO = (1u << 4) | (kFmt << 7) | (kFmt << 10) | (1u << 16) | ((uint32_t)(D >> 3) << 17) |
                                  ((uint32_t)(kQRows >> 4) << 24);
-    const bool leader = (threadIdx.x & 31) == 0;
     const int lane = threadIdx.x & 31;
+    const bool leader = lane == 0;
     const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
     const uint32_t ring = smem_u32(c.base + C::kOffRing);
     uint64_t* const full = c.bar.full;
     uint64_t* const empty = c.bar.empty;
 
-    auto issue_s = [&](int t, uint32_t slot) {
-        const uint32_t a0 = q_smem + t * C::kQTileBytes;
-        const uint32_t b0 = ring + slot * C::kKvTileBytes;
+    // descriptor words: only the low word (start address) moves between MMAs
+    constexpr uint32_t kHi = sdesc_hi_sw128(1024);                 // 8 rows x 128 B per core group
+    const uint32_t q_lo = sdesc_lo(q_smem, 16);                    // K-major: LBO unused
+    const uint32_t k_lo = sdesc_lo(ring, 16);
+    const uint32_t v_lo = sdesc_lo(ring, C::kHalfBytes);           // MN-major: LBO = next 64 columns of d
+    constexpr uint32_t kStageW = C::kKvTileBytes >> 4;             // descriptor units per ring stage
+    constexpr uint32_t kQTileW = C::kQTileBytes >> 4;
+    constexpr uint32_t kHalfW = C::kHalfBytes >> 4;
+
+    auto issue_s = [&](uint32_t qb, int t, uint32_t slot) {
+        const uint32_t a0 = q_lo + (qb * kQTiles + t) * kQTileW;
+        const uint32_t b0 = k_lo + slot * kStageW;
         const uint32_t d = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (uint32_t)((k / 4) * C::kHalfBytes + (k % 4) * 32);
-            mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS, k > 0 ? 1u : 0u);
+            const uint32_t off = (uint32_t)((k / 4) * kHalfW + (k % 4) * 2);  // 16 elements = 32 B
+            mma_ss_w(d, a0 + off, b0 + off, kHi, kIdescS, k > 0 ? 1u : 0u);
         }
     };
-    auto issue_pv = [&](int t, uint32_t slot, bool acc) {
-        const uint32_t b0 = ring + slot * C::kKvTileBytes;
+    // P V over keys 64 * half .. 64 * half + 63
+    auto issue_pv = [&](int t, int half, uint32_t slot, bool acc) {
+        const uint32_t b0 = v_lo + slot * kStageW;
         const uint32_t d = c.tmem + (uint32_t)(C::kOCol + t * D);
         const uint32_t a = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
-        for (int k = 0; k < kKvTile / 16; ++k)
-            mma_ts(d, a + (uint32_t)(k * 8), sdesc_sw128(b0 + (uint32_t)(k * 16 * 128), C::kHalfBytes, 1024), kIdescO,
-                   (acc || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kKvTile / 32; ++kk) {
+            const int k = half * (kKvTile / 32) + kk;                  // 16 keys = 16 rows of 128 B
+            mma_ts_w(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
+        }
     };
     auto wait_full = [&](uint32_t r) -> bool {
         return wait_bar(&full[r % C::kStages], (r / C::kStages) & 1, c.abort_flag, p.err);
@@ -254,31 +309,30 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
 
     uint32_t ring_idx = 0;
     uint32_t p_cnt[kQTiles] = {0, 0};
-    int item_iter = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
+    for (uint32_t n = 0; ok; ++n) {
+        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
+        if (w < 0)
+            break;
         const ItemInfo it = read_item(p, w);
         const int nq = it.g.nq;
-        if (!wait_bar(FP8 ? c.bar.q_conv : c.bar.q_full, item_iter & 1, c.abort_flag, p.err)) {
-            ok = false;
+        const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
+        // TMA (and converter) writes reach the MMA through the mbarrier alone:
+        // no tcgen05 fence is needed after these waits
+        if (!wait_bar(FP8 ? &c.bar.q_conv[qb] : &c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
-        }
-        tc_fence_after();
         // S for the first kv tile
         const uint32_t rk = ring_idx++;
-        if (!wait_full(rk)) {
-            ok = false;
+        if (!wait_full(rk))
             break;
-        }
-        tc_fence_after();
         if (leader) {
             for (int t = 0; t < nq; ++t) {
-                issue_s(t, rk % C::kStages);
+                issue_s(qb, t, rk % C::kStages);
                 mma_commit(&c.bar.s_full[t]);
             }
             mma_commit(&empty[rk % C::kStages]);
             if (it.g.n_lo == it.g.n_hi)
-                mma_commit(c.bar.q_empty);
+                mma_commit(&c.bar.q_empty[qb]);
         }
         __syncwarp();
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
@@ -289,12 +343,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 ok = false;
                 break;
             }
-            tc_fence_after();
             if (!FP8) {
                 // keys >= kv_len: V rows may hold any bits (or a page that was not
                 // loaded); zero them so that P = 0 there cannot meet a NaN.
-                const int k0 = j * kKvTile;
-                const int r0 = it.kv_len - k0;
+                const int r0 = it.kv_len - j * kKvTile;
                 if (r0 < kKvTile) {
                     uint8_t* vt = c.base + C::kOffRing + (rv % C::kStages) * C::kKvTileBytes;
                     const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
@@ -308,14 +360,20 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 }
             }
             for (int t = 0; ok && t < nq; ++t) {
-                if (!wait_bar(&c.bar.p_full[t], p_cnt[t] & 1, c.abort_flag, p.err)) {
-                    ok = false;
-                    break;
+                for (int half = 0; half < 2; ++half) {
+                    if (!wait_bar(&c.bar.p_full[2 * t + half], p_cnt[t] & 1, c.abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (leader)
+                        issue_pv(t, half, rv % C::kStages, j > it.g.n_lo);
+                    __syncwarp();
                 }
+                if (!ok)
+                    break;
                 ++p_cnt[t];
-                tc_fence_after();
                 if (leader) {
-                    issue_pv(t, rv % C::kStages, j > it.g.n_lo);
                     if (t == nq - 1)
                         mma_commit(&empty[rv % C::kStages]);
                     if (last)
@@ -328,15 +386,14 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
                     }
                     if (leader) {
-                        issue_s(t, rk2 % C::kStages);
+                        issue_s(qb, t, rk2 % C::kStages);
                         mma_commit(&c.bar.s_full[t]);
                         if (t == nq - 1) {
                             mma_commit(&empty[rk2 % C::kStages]);
                             if (j + 1 == it.g.n_hi)
-                                mma_commit(c.bar.q_empty);
+                                mma_commit(&c.bar.q_empty[qb]);
                         }
                     }
                     __syncwarp();
@@ -344,7 +401,6 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
             }
         }
     }
-    (void)lane;
     // every MMA this thread issued has completed once the drain barrier flips
     if (leader)
         mma_commit(c.bar.drain);
@@ -356,6 +412,13 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
 // Softmax / correction / epilogue for query tile t: warps 4+4t .. 7+4t, one
 // thread per TMEM lane (= MMA row).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <int D, bool FP8>
 __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 {
@@ -374,7 +437,10 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
+        if (w < 0)
+            break;
         const ItemInfo it = read_item(p, w);
         if (t >= it.g.nq)
             continue;
@@ -420,10 +486,17 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                         s[k] = -INFINITY;
                 }
             }
-            float mx = s[0];
+            // row maximum: eight independent 3-input max chains
+            float pm[8];
 #pragma unroll
-            for (int k = 1; k < kKvTile; ++k)
-                mx = fmaxf(mx, s[k]);
+            for (int a = 0; a < 8; ++a) {
+                float m = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
+#pragma unroll
+                for (int k = 3; k < 15; k += 2)
+                    m = fmax3(m, s[16 * a + k], s[16 * a + k + 1]);
+                pm[a] = fmaxf(m, s[16 * a + 15]);
+            }
+            const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
             const float m_tile = mx * sl2;
             // keep a stale maximum until the row maximum grows by more than 2^8:
             // exact, since the denominator uses the same stale maximum
@@ -435,47 +508,57 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                 m_used = m_tile;
             }
             const float neg = m_used == -INFINITY ? 0.f : -m_used;
-            float rs0 = 0.f, rs1 = 0.f;
-            uint32_t pk[kKvTile / 2];
+            const float2 sc = make_float2(sl2, sl2), ng = make_float2(neg, neg);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            const bool rescale = __any_sync(0xffffffffu, need) && j > it.g.n_lo;
 #pragma unroll
-            for (int k = 0; k < kKvTile / 2; ++k) {
-                const float p0 = ex2_approx(fmaf(s[2 * k], sl2, neg));
-                const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, neg));
-                rs0 += p0;
-                rs1 += p1;
-                if (FP8) {
-                    uint32_t r;
-                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));
-                    pk[k] = r;
-                } else {
-                    pk[k] = pack_bf16x2(p0, p1);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const int k = half * 32 + kk;
+                    const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
+                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
+                    if (FP8) {
+                        uint32_t r;
+                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
+                        pk[kk] = r;
+                    } else {
+                        pk[kk] = pack_bf16x2(e.x, e.y);
+                    }
                 }
-            }
-            l += rs0 + rs1;
-            {
-                uint32_t (&pa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-                uint32_t (&pb)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-                tmem_st32(s_tmem, pa);
-                tmem_st32(s_tmem + 32, pb);
-            }
-            if (__any_sync(0xffffffffu, need) && j > it.g.n_lo) {
-                const float a = need ? alpha : 1.f;
+                if (half == 0 && rescale) {
+                    // O holds this item's sum up to tile j-1 (S(j) was issued after
+                    // PV(j-1)); rescale it before the first P V of tile j
+                    const float f = need ? alpha : 1.f;
+                    const float2 ff = make_float2(f, f);
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
-                    tmem_wait_ld();
+                    for (int q = 0; q < D / 16; ++q) {
+                        uint32_t o[16];
+                        tmem_ld16(o_tmem + (uint32_t)(q * 16), o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
-                    tmem_st32(o_tmem + (uint32_t)(q * 32), o);
+                        for (int k = 0; k < 16; k += 2) {
+                            const float2 v =
+                                __fmul2_rn(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), ff);
+                            o[k] = __float_as_uint(v.x);
+                            o[k + 1] = __float_as_uint(v.y);
+                        }
+                        tmem_st16(o_tmem + (uint32_t)(q * 16), o);
+                    }
                 }
+                tmem_st32(s_tmem + (uint32_t)(half * 32), pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&c.bar.p_full[2 * t + half]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c.bar.p_full[t]);
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a = __fadd2_rn(a01, a23);
+            l += a.x + a.y;
         }
         if (!ok)
             break;
@@ -491,6 +574,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         if (p.sinks != nullptr && m_used != -INFINITY && row_real)
             total += ex2_approx(fmaf(p.sinks[h], kLog2e, -m_used));
         const float inv = (m_used != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
+        const float2 inv2 = make_float2(inv, inv);
         uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -498,16 +582,17 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
             tmem_wait_ld();
             if (valid) {
+                uint32_t pkd[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float2 v =
+                        __fmul2_rn(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), inv2);
+                    pkd[k] = pack_bf16x2(v.x, v.y);
+                }
                 uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 pk4;
-                    pk4.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                    pk4.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                    pk4.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                    pk4.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                    dst[v] = pk4;
-                }
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
             }
         }
     }
@@ -542,16 +627,17 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
     const int lane = threadIdx.x & 31;
     const int sw = ct & 7;                 // 128-byte swizzle phase of this row
     uint32_t r8 = 0, r = 0;
-    int item_iter = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < c.n_items; w += gridDim.x, ++item_iter) {
-        const ItemInfo it = read_item(p, w);
-        if (!wait_bar(c.bar.q_full, item_iter & 1, c.abort_flag, p.err)) {
-            ok = false;
+    for (uint32_t n = 0; ok; ++n) {
+        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
+        if (w < 0)
             break;
-        }
+        const ItemInfo it = read_item(p, w);
+        const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
+        if (!wait_bar(&c.bar.q_full[qb], qph, c.abort_flag, p.err))
+            break;
         for (int t = 0; t < it.g.nq; ++t) {
-            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + t * C::kQTileBytes);
+            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + (qb * kQTiles + t) * C::kQTileBytes);
             for (int k = ct; k < C::kQTileBytes / 16; k += 128) {
                 uint4 v = q[k];
                 v.x = bf16x2_to_f16x2(v.x);
@@ -564,7 +650,7 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(c.bar.q_conv);
+            mbar_arrive(&c.bar.q_conv[qb]);
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
             const bool zero = j * kKvTile + ct >= it.kv_len;
             for (int kind = 0; kind < 2; ++kind) {
@@ -620,18 +706,21 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     Ctx c;
     c.base = base;
     c.bar.full = bars;
-    c.bar.empty = bars + C::kStages;
+    c.bar.empty = c.bar.full + C::kStages;
     c.bar.f8full = c.bar.empty + C::kStages;
     c.bar.f8empty = c.bar.f8full + C::kF8Stages;
     c.bar.q_full = c.bar.f8empty + C::kF8Stages;
-    c.bar.q_empty = c.bar.q_full + 1;
-    c.bar.q_conv = c.bar.q_full + 2;
-    c.bar.s_full = c.bar.q_full + 3;
+    c.bar.q_empty = c.bar.q_full + C::kQBufs;
+    c.bar.q_conv = c.bar.q_empty + C::kQBufs;
+    c.bar.s_full = c.bar.q_conv + C::kQBufs;
     c.bar.p_full = c.bar.s_full + kQTiles;
-    c.bar.o_full = c.bar.p_full + kQTiles;
+    c.bar.o_full = c.bar.p_full + 2 * kQTiles;
     c.bar.drain = c.bar.o_full + kQTiles;
+    c.bar.it_full = c.bar.drain + 1;
+    c.bar.it_empty = c.bar.it_full + C::kItemSlots;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
     c.abort_flag = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
+    c.item_slot = reinterpret_cast<volatile int*>(base + C::kOffMisc + 16);
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
@@ -643,15 +732,22 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             mbar_init(&c.bar.f8full[s], 1);
             mbar_init(&c.bar.f8empty[s], 4);
         }
-        mbar_init(c.bar.q_full, 1);
-        mbar_init(c.bar.q_empty, 1);
-        mbar_init(c.bar.q_conv, 4);
+        for (int b = 0; b < C::kQBufs; ++b) {
+            mbar_init(&c.bar.q_full[b], 1);
+            mbar_init(&c.bar.q_empty[b], 1);
+            mbar_init(&c.bar.q_conv[b], 4);
+        }
         for (int t = 0; t < kQTiles; ++t) {
             mbar_init(&c.bar.s_full[t], 1);
-            mbar_init(&c.bar.p_full[t], 4);
+            mbar_init(&c.bar.p_full[2 * t], 4);
+            mbar_init(&c.bar.p_full[2 * t + 1], 4);
             mbar_init(&c.bar.o_full[t], 1);
         }
         mbar_init(c.bar.drain, 1);
+        for (int s = 0; s < C::kItemSlots; ++s) {
+            mbar_init(&c.bar.it_full[s], 1);
+            mbar_init(&c.bar.it_empty[s], C::kItemConsumerWarps);
+        }
         *c.abort_flag = 0;
         fence_mbar_init();
     }
@@ -670,7 +766,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         const int pad = C::kHalfBytes - used;
         if (pad > 0) {
             const int n16 = pad / 16;
-            for (int k = threadIdx.x; k < kQTiles * C::kHalves * n16; k += blockDim.x) {
+            for (int k = threadIdx.x; k < C::kQBufs * kQTiles * C::kHalves * n16; k += blockDim.x) {
                 const int blk = k / n16, q = k % n16;
                 *reinterpret_cast<uint4*>(base + C::kOffQ + blk * C::kHalfBytes + used + q * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
@@ -683,15 +779,15 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     tc_fence_after();
     c.tmem = *tmem_holder;
 
-    // the work list is written by the scheduler kernel that precedes this one
+    // the work list and the counter are written by the scheduler kernel that precedes this one
     pdl_wait();
     c.n_items = min(*p.count, p.cap);
 
     if constexpr (FP8) {
         // 512 threads launch with 128 registers each; the softmax warpgroups
-        // take registers from the others (56 + 184 + 184 + 80 = 504 <= 4 x 128)
+        // take registers from the others (64 + 184 + 184 + 80 = 512 = 4 x 128)
         if (warp < 4) {
-            regs_dec<56>();
+            regs_dec<64>();
             if (warp == 0)
                 producer_role<D, FP8>(p, c);
             else if (warp == 1)
@@ -704,12 +800,17 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             convert_role<D, FP8>(p, c);
         }
     } else {
-        if (warp == 0)
-            producer_role<D, FP8>(p, c);
-        else if (warp == 1)
-            mma_role<D, FP8>(p, c);
-        else if (warp >= 4)
+        // 384 threads launch with 168 registers each (64 + 216 + 216 = 496 <= 3 x 168)
+        if (warp < 4) {
+            regs_dec<64>();
+            if (warp == 0)
+                producer_role<D, FP8>(p, c);
+            else if (warp == 1)
+                mma_role<D, FP8>(p, c);
+        } else {
+            regs_inc<216>();
             softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+        }
     }
 
     tc_fence_before();
@@ -725,12 +826,14 @@ static cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream
 {
     using C = TcCfg<D, FP8>;
     auto kern = attention_tc_kernel<D, FP8>;
-    static bool attr_done = false;
-    if (!attr_done) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static unsigned long long attr_done = 0;  // one bit per device
+    if (dev < 64 && !(attr_done & (1ull << dev))) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess)
             return e;
-        attr_done = true;
+        attr_done |= 1ull << dev;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

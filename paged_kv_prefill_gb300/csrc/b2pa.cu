@@ -23,6 +23,8 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<int> g_path{B2PA_PATH_AUTO};
 std::atomic<int> g_debug{0};
+std::atomic<void*> g_ev_start{nullptr};
+std::atomic<void*> g_ev_stop{nullptr};
 
 int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int status, const char* fmt, ...)
@@ -75,7 +77,7 @@ int device_info(int* dev_out, DevInfo* info)
 
 // ------------------------------------------------------------------ workspaces
 
-// Per (device, stream): [0] error word, [4] item count, [256 ..) work items.
+// Per (device, stream): [0] error word, [4] item count, [8] work counter, [256 ..) work items.
 struct Workspace {
     int dev;
     cudaStream_t stream;
@@ -420,6 +422,7 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     sp.cap = (int)cap;
     sp.items = reinterpret_cast<int4*>(ws.mem + kWsHeader);
     sp.count = reinterpret_cast<int*>(ws.mem + 4);
+    sp.counter = reinterpret_cast<int*>(ws.mem + 8);
     sp.err = reinterpret_cast<unsigned*>(ws.mem);
     return sp;
 }
@@ -486,6 +489,7 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
             ap.out_stride_head = pr.out_st_head;
             ap.items = sp.items;
             ap.count = sp.count;
+            ap.counter = sp.counter;
             ap.err = sp.err;
             ap.cap = (int)cap;
             ap.H = pr.H;
@@ -497,9 +501,16 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
             ap.window = window;
             ap.scale_log2 = scale_log2;
             ap.bmm2 = bmm2_scale;
-            e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true);
+            cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_ev_start.load());
+            cudaEvent_t ev1 = static_cast<cudaEvent_t>(g_ev_stop.load());
+            const bool timed = ev0 != nullptr && ev1 != nullptr;
+            if (timed && (e = cudaEventRecord(ev0, stream)) != cudaSuccess)
+                return cuda_fail(e, "cudaEventRecord");
+            e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, !timed);
             if (e != cudaSuccess)
                 return cuda_fail(e, "attention kernel launch");
+            if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
+                return cuda_fail(e, "cudaEventRecord");
             return B2PA_OK;
         }
     }
@@ -737,6 +748,14 @@ int b2pa_query_path(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_
     if ((st = choose_path(pr, di, &use_tc)))
         return st;
     return use_tc ? B2PA_PATH_TCGEN05 : B2PA_PATH_GENERIC;
+}
+
+int b2pa_set_timing_events(void* start_event, void* stop_event)
+{
+    const bool on = start_event != nullptr && stop_event != nullptr;
+    g_ev_start.store(on ? start_event : nullptr);
+    g_ev_stop.store(on ? stop_event : nullptr);
+    return B2PA_OK;
 }
 
 int b2pa_set_debug_checks(int32_t on)

@@ -16,7 +16,7 @@ constexpr int kQTiles = 2;        // query tiles per work item (they share every
 constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
-constexpr int kSchedMaxBatch = 16384;
+constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 3 ints per request in shared memory
 constexpr long long kWaitLimitCycles = 1LL << 31;  // ~1 s at 2 GHz: a pipeline wait that exceeds this gives up
 
 // A request is processed only if its lengths are consistent with the bounds
@@ -79,6 +79,7 @@ struct SchedParams {
     int cap;
     int4* items;
     int* count;
+    int* counter;             // work counter of the attention kernel, reset here
     unsigned* err;
 };
 
@@ -96,6 +97,7 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     long long out_stride_head;
     const int4* items;
     const int* count;
+    int* counter;        // next work item (atomicAdd); zero at launch
     unsigned* err;
     int cap;
     int H, Hkv, G, rows_per_tile, page_size, num_pages;

@@ -57,12 +57,17 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     // let the attention kernel start its prologue while the list is built
     pdl_launch_dependents();
     extern __shared__ int sm[];
+    const int B = p.B;
     int* hist = sm;                                  // [32 warps][kSchedBuckets]
     int* scratch = hist + 32 * kSchedBuckets;        // 64
-    int* req_start = scratch + 64;                   // [B + 1] first item of each request
+    int* tot = scratch + 64;                         // [kSchedBuckets]
+    int* req_start = tot + kSchedBuckets;            // [B + 1] first item of each request
+    int* req_q = req_start + B + 1;                  // [B] q_len
+    int* req_kv = req_q + B;                         // [B] kv_len
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per_item = p.rows_per_tile * kQTiles;
-    const int B = p.B;
+    if (tid == 0)
+        *p.counter = 0;
 
     // 1. per-request item counts, as a block-wide scan over contiguous chunks
     const int chunk = (B + kSchedThreads - 1) / kSchedThreads;
@@ -75,6 +80,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
         const int n = (r.ok && r.q_len > 0) ? p.Hkv * ((r.q_len + per_item - 1) / per_item) : 0;
         req_start[b] = n;  // count for now
+        req_q[b] = r.q_len;
+        req_kv[b] = r.kv_len;
         local += n;
         if (p.debug) {
             if (p.cum_kv != nullptr && r.ok && p.cum_kv[b + 1] - p.cum_kv[b] != r.kv_len)
@@ -89,6 +96,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             }
         }
     }
+    for (int k = tid; k < 32 * kSchedBuckets; k += kSchedThreads)
+        hist[k] = 0;
     int n_total = 0;
     int run = block_exclusive_scan(local, scratch, &n_total);
     for (int b = b_begin; b < b_end; ++b) {
@@ -96,13 +105,12 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         req_start[b] = run;
         run += n;
     }
-    if (tid == 0)
+    if (tid == 0) {
         req_start[B] = n_total;
-    for (int k = tid; k < 32 * kSchedBuckets; k += kSchedThreads)
-        hist[k] = 0;
+        if (n_total > p.cap)
+            atomicOr(p.err, (unsigned)B2PA_DEV_OVERFLOW);
+    }
     __syncthreads();
-    if (n_total > p.cap && tid == 0)
-        atomicOr(p.err, (unsigned)B2PA_DEV_OVERFLOW);
 
     // item idx -> (b, kv head, it, bucket)
     auto decode = [&](int idx, int4& item, int& bucket) {
@@ -115,8 +123,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
                 hi = mid - 1;
         }
         const int b = lo;
-        const int q_len = p.cum_q[b + 1] - p.cum_q[b];
-        const int kv_len = p.seq_lens[b];
+        const int q_len = req_q[b];
+        const int kv_len = req_kv[b];
         const int n_it = (q_len + per_item - 1) / per_item;
         const int loc = idx - req_start[b];
         const int kvh = loc / n_it, it = loc % n_it;
@@ -145,7 +153,6 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     __syncthreads();
 
     // 3. offsets: buckets in descending order, warps in ascending order
-    int bucket_total = 0;
     {
         const int c = tid;  // kSchedBuckets == kSchedThreads
         int acc = 0;
@@ -154,16 +161,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             hist[w * kSchedBuckets + c] = acc;
             acc += v;
         }
-        bucket_total = acc;
+        tot[c] = acc;
     }
     __syncthreads();
     // exclusive scan over buckets from the top: thread t takes bucket kCostCap - t
-    int* tot = req_start + B + 1;  // [kSchedBuckets] scratch after req_start
-    tot[tid] = bucket_total;
-    __syncthreads();
-    const int mine = tot[kCostCap - tid];
-    __syncthreads();
-    const int start = block_exclusive_scan(mine, scratch, nullptr);
+    const int start = block_exclusive_scan(tot[kCostCap - tid], scratch, nullptr);
     {
         const int c = kCostCap - tid;
         for (int w = 0; w < 32; ++w)
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
 {
-    const size_t smem = sizeof(int) * ((size_t)32 * kSchedBuckets + 64 + (size_t)p.B + 1 + kSchedBuckets);
+    const size_t smem = sizeof(int) * ((size_t)32 * kSchedBuckets + 64 + kSchedBuckets + 3 * (size_t)p.B + 1);
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
