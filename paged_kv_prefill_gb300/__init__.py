@@ -200,7 +200,7 @@ def debug_worklist(query, k_pool, block_tables, seq_lens, cum_seq_lens_q, max_q_
     lib = load()
     H = query.shape[1]
     Hkv = k_pool.shape[1] if kv_layout == "HND" else k_pool.shape[2]
-    per = 2 * (128 // (H // Hkv))
+    per = 128 // (H // Hkv)  # tokens of one query tile: an item holds at least one
     cap = max(1, seq_lens.numel() * Hkv * ((max(max_q_len, 1) + per - 1) // per))
     items = np.zeros((cap, 4), dtype=np.int32)
     n = ctypes.c_int32(0)

@@ -12,12 +12,12 @@ namespace b2pa {
 
 constexpr int kKvTile = 128;      // keys per kv tile (MMA N of Q K^T, K of P V)
 constexpr int kQRows = 128;       // MMA M rows per query tile (tokens x heads of one kv group)
-constexpr int kQTiles = 2;        // query tiles per work item (they share every K/V tile)
+constexpr int kQTiles = 1;        // query tiles per work item
 constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 3 ints per request in shared memory
-constexpr long long kWaitLimitCycles = 1LL << 31;  // ~1 s at 2 GHz: a pipeline wait that exceeds this gives up
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait that exceeds this gives up
 
 // A request is processed only if its lengths are consistent with the bounds
 // the caller gave; otherwise the scheduler sets B2PA_DEV_BAD_REQUEST.

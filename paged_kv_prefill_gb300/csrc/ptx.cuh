@@ -54,6 +54,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// ---------------------------------------------------------------- named barriers (PTX ISA: bar.sync)
+
+// Barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier `id` over `nthreads` threads that also ANDs a predicate across them
+// (PTX ISA: barrier.cta.red): every thread gets the same result.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.b32 pi, %1, 0;\n\t"
+        "barrier.cta.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- proxy fences
 
 // Order this thread's generic-proxy shared-memory writes before later
@@ -291,6 +313,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Global nanosecond timer (PTX ISA: %globaltimer).  Unlike the per-SM cycle
+// counter it is one clock for the whole GPU, so a bounded wait measured with it
+// does not fire early if a CTA is suspended and resumed.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 __device__ __forceinline__ uint32_t lane_id()

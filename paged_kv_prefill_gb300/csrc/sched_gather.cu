@@ -266,9 +266,9 @@ __global__ void __launch_bounds__(128) gather_kernel(const __grid_constant__ Gat
                     tma_load_4d(dst + h * half_bytes, kind ? &p.tm_v : &p.tm_k, bar, h * 64, slot0, kvh, page);
             }
         }
-        const long long t0 = clock64();
+        const uint64_t t0 = global_ns();
         while (!mbar_try_wait(smem_u32(bar), kind)) {
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (global_ns() - t0 > kWaitLimitNs) {
                 if (threadIdx.x == 0)
                     atomicOr(p.err, (unsigned)B2PA_DEV_TIMEOUT);
                 break;

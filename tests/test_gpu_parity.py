@@ -333,3 +333,26 @@ def test_invalid_arguments_rejected_on_host(cuda_lib):
         q3 = d["q"][:, :3]
         cuda_lib.context_attention(q3, (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], 4, 8, 0.1,
                                    1.0, d["cum_q"], None, -1, None, "HND")
+
+
+@pytest.mark.parametrize("which", ["ragged_lone_tiles", "cfg2", "cfg5"])
+def test_stress_back_to_back_calls(cuda_lib, which):
+    """Hundreds of calls in a row (the pattern a timed benchmark produces): no
+    device error bit, and the last output still matches the oracle."""
+    if which == "cfg2":
+        inp = workload.config(2)
+    elif which == "cfg5":
+        inp = workload.config(5)
+    else:
+        ql = [1, 33, 64, 65, 97, 7, 128, 31, 200, 3]
+        kl = [900, 33, 1000, 65, 2000, 7, 300, 1500, 200, 3000]
+        inp = workload.build(ql, kl, 32, 8, 128, 32, "HND", seed=21, with_sinks=True)
+    d = _to_dev(inp)
+    out = torch.zeros_like(d["q"])
+    for _ in range(300 if which != "cfg5" else 60):
+        cuda_lib.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                   inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"],
+                                   d["cum_kv"], inp.window_left, out, inp.layout, d["sinks"])
+    assert cuda_lib.device_status() == 0
+    rows = _sample_rows(inp, 300, seed=5)
+    _compare(out, inp, rows=rows)
