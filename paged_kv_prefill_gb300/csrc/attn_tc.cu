@@ -9,34 +9,36 @@
 // One CTA per SM.  Work items come from the scheduler's longest-first list;
 // the producer warp takes the next one with an atomic counter and hands its
 // index to the other roles through a small shared-memory ring.  A work item
-// is (request b, kv head, query tile): 128 MMA rows, a row being one (token,
-// query head) pair of the kv head's group (rows_per_tile tokens x G heads),
-// streamed against the request's K/V tiles of 128 keys.
+// is (request b, kv head, item index): two query tiles of 128 MMA rows, a row
+// being one (token, query head) pair of the kv head's group (rows_per_tile
+// tokens x G heads).  Both query tiles stream the same K/V tiles of 128 keys.
 //
 //   warp 0        producer: item fetch; TMA loads of Q (3-D map, double
-//                 buffered across items) and of K/V pages (4-D map, one box
-//                 per page and 128-byte column block) through a ring of
-//                 stages with full/empty mbarriers.
-//   warp 1        MMA issuer (one lane) and TMEM owner.  Per kv tile j it
-//                 issues O += P(j) V(j) and then S(j+2) = Q K(j+2)^T: S is
-//                 double buffered in TMEM, so S(j+1) is computed while the
-//                 softmax of tile j runs.
-//   warp 2        (16-bit KV) zeroes V rows past kv_len in the last kv tile of
-//                 a request, then releases every V tile to the MMAs.
-//   warps 4-7     softmax of keys 0-63 of every S tile, one thread per row;
-//   warps 8-11    softmax of keys 64-127.  The two warpgroups exchange row
-//                 maxima through shared memory, so both use one stabiliser
-//                 per row; each rescales and writes back its half of the O
-//                 columns.
+//                 buffered across items where shared memory allows) and of
+//                 K/V pages (4-D map, one box per page and 128-byte column
+//                 block) through a ring of stages with full/empty mbarriers.
+//   warp 1        MMA issuer (one lane): S_t = Q_t K^T into TMEM, then
+//                 O_t += P_t V with P_t read from TMEM, for t = 0, 1, in the
+//                 order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) so the tensor
+//                 core works on one tile while the other tile's softmax runs.
+//                 Owns the TMEM allocation.
+//   warps 4-7     softmax of query tile 0 (one thread per row), O rescale,
+//                 and the epilogue (bmm2_scale / denominator, bf16 stores).
+//   warps 8-11    the same for query tile 1.
 //   warps 12-15   (FP8 KV only) convert e4m3 K/V tiles to f16 in the MMA
-//                 layout (zeroing rows past kv_len), and Q from bf16 to f16.
+//                 layout, and the Q tile from bf16 to f16.
 //
-// TMEM (512 columns): S buffers at [0,128) and [128,256), O at [256,256+D).
-// P (16-bit, two per column) overwrites the first 64 columns of its S buffer.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P_t (16-bit, two per column) overwrites the first 64 columns of S_t; it is
+// handed to the MMA warp in two halves (keys 0-63, 64-127) so that P V on the
+// first half overlaps the softmax of the second.
 //
-// Every wait is bounded: after kWaitLimitNs (2 s of %globaltimer) the CTA
-// raises B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies
-// and MMAs are drained, and TMEM is freed before the CTA exits.
+// The row maximum of an S tile comes with its TMEM load (tcgen05.ld.red, an
+// sm_103a instruction) except on tiles that need masking.
+//
+// Every wait is bounded: after kWaitLimitNs (2 s of %globaltimer) the CTA raises
+// B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies and
+// MMAs are drained, and TMEM is freed before the CTA exits.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -48,31 +50,27 @@ struct TcCfg {
     static constexpr int kHalfBytes = kQRows * 128;   // one column block of a 128-row tile
     static constexpr int kQTileBytes = kHalves * kHalfBytes;
     static constexpr int kKvTileBytes = kHalves * kHalfBytes;
-    // The last Q K^T of an item is issued two kv tiles before its end, so a
-    // single Q buffer already leaves that long for the next item's Q to land.
-    static constexpr int kQBufs = D == 128 ? 1 : 2;                 // Q tiles in flight (items)
+    // A kv tile j is in use from S(j) to PV(j); the ring must also hold the
+    // next K and V in flight: at least 4 stages, 5 where shared memory allows.
+    static constexpr int kQBufs = D == 128 ? 1 : 2;                 // Q buffers (items in flight)
     static constexpr int kStages = D == 128 ? (FP8 ? 4 : 5) : 8;    // 16-bit K/V ring
     static constexpr int kF8Stages = FP8 ? 2 : 0;                   // e4m3 staging ring
-    static constexpr int kF8TileBytes = kKvTile * D;                // e4m3 tile: 128 rows of D bytes
+    static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
     static constexpr int kThreads = FP8 ? 512 : 384;
-    static constexpr int kSoftThreads = 256;                        // warps 4-11
     static constexpr int kItemSlots = 4;
-    static constexpr int kItemConsumerWarps = 1 + 8 + (FP8 ? 4 : 1);
-    static constexpr int kVReady = FP8 ? 0 : kStages;               // V-release ring (16-bit KV)
+    static constexpr int kItemConsumerWarps = 1 + 8 + (FP8 ? 4 : 0);
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 2 * kKvTile;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffRing = kOffQ + kQBufs * kQTileBytes;
+    static constexpr int kOffRing = kOffQ + kQBufs * kQTiles * kQTileBytes;
     static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
-    static constexpr int kOffXchg = kOffF8 + kF8Stages * kF8TileBytes;  // row maxima [2 tiles][2 halves][128], sums [2][128]
-    static constexpr int kXchgBytes = (2 * 2 * kQRows + 2 * kQRows) * 4;
-    static constexpr int kOffBar = kOffXchg + kXchgBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + kVReady + 3 * kQBufs + 2 + 2 + 2 + 1 + 4 + 2 * kItemSlots;
+    static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 * kQBufs + 4 * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "fp8 path is D = 128");
-    static_assert(kOCol + D <= kTmemCols, "tmem");
+    static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -81,18 +79,13 @@ struct Bars {
     uint64_t* empty;     // [kStages]  tile consumed by the MMAs
     uint64_t* f8full;    // [kF8Stages]
     uint64_t* f8empty;   // [kF8Stages]
-    uint64_t* vready;    // [kVReady]  (16-bit KV) V tile checked / tail-zeroed, by V sequence number
-    uint64_t* q_full;    // [kQBufs]   Q tile landed
+    uint64_t* q_full;    // [kQBufs]   Q tiles landed
     uint64_t* q_empty;   // [kQBufs]   last Q K^T of the item done
     uint64_t* q_conv;    // [kQBufs]   (FP8) Q converted to f16
-    uint64_t* s_full;    // [2]        S buffer b written
-    uint64_t* p_full;    // [2]        P in S buffer b (8 softmax warps)
-    uint64_t* xch;       // [2]        row maxima of S buffer b posted (8 softmax warps)
-    uint64_t* xsum;      //            row sums of the item posted (8 softmax warps)
-    uint64_t* pv_done;   //            one phase per P V issued (O readable / rescalable)
-    uint64_t* o_full;    //            last P V of the item done
-    uint64_t* o_empty;   //            epilogue finished reading O (8 softmax warps)
-    uint64_t* drain;     //            every MMA done (teardown)
+    uint64_t* s_full;    // [2]        S_t in TMEM
+    uint64_t* p_full;    // [2][2]     half h of P_t in TMEM (4 softmax warps)
+    uint64_t* o_full;    // [2]        last P V of the item done
+    uint64_t* drain;
     uint64_t* it_full;   // [kItemSlots] item index posted
     uint64_t* it_empty;  // [kItemSlots] item index read by every consumer warp
 };
@@ -174,7 +167,6 @@ __device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint
 // ---------------------------------------------------------------------------
 // Producer: warp 0.  Lane 0 takes items; lane l loads page l of a kv tile (one
 // TMA box per 128-byte column block) after lane 0 posted the byte count.
-// Ring order: K(lo), V(lo), K(lo+1), V(lo+1), ...
 // ---------------------------------------------------------------------------
 template <int D, bool FP8>
 __device__ void producer_role(const AttnParams& p, const Ctx& c)
@@ -212,16 +204,18 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         if (w < 0)
             break;
         const ItemInfo it = read_item(p, w);
-        // the Q tile, into its buffer once the last item that used it has finished with it
+        // Q tiles, into the buffer of this item once its previous user is done
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c.abort_flag, p.err))
             break;
         if (lane == 0)
-            mbar_arrive_expect_tx(&c.bar.q_full[qb], (uint32_t)C::kHalves * q_box_bytes);
+            mbar_arrive_expect_tx(&c.bar.q_full[qb], (uint32_t)(it.g.nq * C::kHalves) * q_box_bytes);
         __syncwarp();
-        if (lane < C::kHalves)
-            tma_load_3d(q_smem + qb * C::kQTileBytes + lane * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb], lane * 64,
-                        it.kvh * p.G, it.q0 + it.g.tok0);
+        if (lane < it.g.nq * C::kHalves) {
+            const int t = lane / C::kHalves, h = lane % C::kHalves;
+            tma_load_3d(q_smem + (qb * kQTiles + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
+                        h * 64, it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
+        }
         const int* bt_row = p.block_tables + (long long)it.b * p.bt_stride;
         const int n_pages_valid = (it.kv_len + P - 1) / P;
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
@@ -263,55 +257,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
 }
 
 // ---------------------------------------------------------------------------
-// V release (16-bit KV): warp 2.  For every kv tile, in ring order: wait for
-// its K and V to land (K too, although this warp does not touch it: a parity
-// wait is only sound once every earlier phase of the same slot has been
-// observed, and TMA copies may land out of issue order), zero the V rows at
-// keys >= kv_len (they may hold any bits, or a page that was not loaded, and
-// P = 0 there must not meet a NaN), then arrive on vready[v % kVReady].
-// ---------------------------------------------------------------------------
-template <int D, bool FP8>
-__device__ void vrelease_role(const AttnParams& p, const Ctx& c)
-{
-    using C = TcCfg<D, FP8>;
-    const int lane = threadIdx.x & 31;
-    uint32_t ring_idx = 0, v_idx = 0;
-    bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
-        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
-        if (w < 0)
-            break;
-        const ItemInfo it = read_item(p, w);
-        for (int j = it.g.n_lo; j <= it.g.n_hi; ++j, ring_idx += 2, ++v_idx) {
-            const uint32_t rk = ring_idx, rv = ring_idx + 1;
-            if (!wait_bar(&c.bar.full[rk % C::kStages], (rk / C::kStages) & 1, c.abort_flag, p.err) ||
-                !wait_bar(&c.bar.full[rv % C::kStages], (rv / C::kStages) & 1, c.abort_flag, p.err)) {
-                ok = false;
-                break;
-            }
-            const int r0 = it.kv_len - j * kKvTile;
-            if (r0 < kKvTile) {
-                uint8_t* vt = c.base + C::kOffRing + (rv % C::kStages) * C::kKvTileBytes;
-                const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
-                for (int h = 0; h < C::kHalves; ++h) {
-                    uint4* dst = reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + r0 * 128);
-                    for (int q = lane; q < n16; q += 32)
-                        dst[q] = make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c.bar.vready[v_idx % C::kVReady]);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // MMA issuer: warp 1, lane 0 issues; the whole warp waits.
-// Tile g (counted over all items of the CTA) uses S buffer g & 1.  Order:
-// S(lo), S(lo+1), then per tile j: P V(j), S(j+2).  S(j+2) overwrites P(j)
-// only after P V(j) read it, because MMAs of one thread run in issue order.
 // ---------------------------------------------------------------------------
 template <int D, bool FP8>
 __device__ void mma_role(const AttnParams& p, const Ctx& c)
@@ -325,106 +271,138 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                                  ((uint32_t)(kQRows >> 4) << 24);
     const int lane = threadIdx.x & 31;
     const bool leader = lane == 0;
-    const uint32_t tmem = __shfl_sync(0xffffffffu, c.tmem, 0);
-    const uint32_t o_col = tmem + (uint32_t)C::kOCol;
-    // shared-memory descriptor words: only the low word (start address) moves
-    constexpr uint32_t kHi = sdesc_hi_sw128(1024);                      // 8 rows x 128 B per core group
-    const uint32_t q_lo = sdesc_lo(smem_u32(c.base + C::kOffQ), 16);    // K-major: LBO unused
-    const uint32_t k_lo = sdesc_lo(smem_u32(c.base + C::kOffRing), 16);
-    const uint32_t v_lo = sdesc_lo(smem_u32(c.base + C::kOffRing), C::kHalfBytes);  // MN-major: LBO = next 64 d
-    constexpr uint32_t kStageW = C::kKvTileBytes >> 4;
+    const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
+    const uint32_t ring = smem_u32(c.base + C::kOffRing);
+    uint64_t* const full = c.bar.full;
+    uint64_t* const empty = c.bar.empty;
+
+    // descriptor words: only the low word (start address) moves between MMAs
+    constexpr uint32_t kHi = sdesc_hi_sw128(1024);                 // 8 rows x 128 B per core group
+    const uint32_t q_lo = sdesc_lo(q_smem, 16);                    // K-major: LBO unused
+    const uint32_t k_lo = sdesc_lo(ring, 16);
+    const uint32_t v_lo = sdesc_lo(ring, C::kHalfBytes);           // MN-major: LBO = next 64 columns of d
+    constexpr uint32_t kStageW = C::kKvTileBytes >> 4;             // descriptor units per ring stage
     constexpr uint32_t kQTileW = C::kQTileBytes >> 4;
     constexpr uint32_t kHalfW = C::kHalfBytes >> 4;
 
-    auto issue_s = [&](uint32_t qb, uint32_t buf, uint32_t slot) {
-        const uint32_t a0 = q_lo + qb * kQTileW;
+    auto issue_s = [&](uint32_t qb, int t, uint32_t slot) {
+        const uint32_t a0 = q_lo + (qb * kQTiles + t) * kQTileW;
         const uint32_t b0 = k_lo + slot * kStageW;
-        const uint32_t d = tmem + buf * (uint32_t)kKvTile;
+        const uint32_t d = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (uint32_t)((k / 4) * kHalfW + (k % 4) * 2);  // 16 elements = 32 B
             mma_ss_w(d, a0 + off, b0 + off, kHi, kIdescS, k > 0 ? 1u : 0u);
         }
     };
-    auto issue_pv = [&](uint32_t buf, uint32_t slot, bool acc) {
+    // P V over keys 64 * half .. 64 * half + 63
+    auto issue_pv = [&](int t, int half, uint32_t slot, bool acc) {
         const uint32_t b0 = v_lo + slot * kStageW;
-        const uint32_t a = tmem + buf * (uint32_t)kKvTile;
+        const uint32_t d = c.tmem + (uint32_t)(C::kOCol + t * D);
+        const uint32_t a = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
-        for (int k = 0; k < kKvTile / 16; ++k)  // 16 keys = 16 rows of 128 B
-            mma_ts_w(o_col, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kKvTile / 32; ++kk) {
+            const int k = half * (kKvTile / 32) + kk;                  // 16 keys = 16 rows of 128 B
+            mma_ts_w(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
+        }
     };
     auto wait_full = [&](uint32_t r) -> bool {
-        return wait_bar(&c.bar.full[r % C::kStages], (r / C::kStages) & 1, c.abort_flag, p.err);
+        return wait_bar(&full[r % C::kStages], (r / C::kStages) & 1, c.abort_flag, p.err);
     };
 
-    uint32_t ring_idx = 0, v_idx = 0, g = 0;
+    uint32_t ring_idx = 0;
+    uint32_t p_cnt[kQTiles] = {0, 0};
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
         const int w = take_item<C::kItemSlots>(p, c, n, &ok);
         if (w < 0)
             break;
         const ItemInfo it = read_item(p, w);
-        const int tiles = it.g.n_hi - it.g.n_lo + 1;
+        const int nq = it.g.nq;
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
-        const uint32_t base = ring_idx;  // K(lo + t) at base + 2t, V at base + 2t + 1
-        ring_idx += 2 * tiles;
         // TMA (and converter) writes reach the MMA through the mbarrier alone:
         // no tcgen05 fence is needed after these waits
         if (!wait_bar(FP8 ? &c.bar.q_conv[qb] : &c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
-        for (int t = 0; ok && t < 2 && t < tiles; ++t) {
-            const uint32_t rk = base + 2 * t;
-            if (!wait_full(rk)) {
-                ok = false;
-                break;
+        // S for the first kv tile
+        const uint32_t rk = ring_idx++;
+        if (!wait_full(rk))
+            break;
+        if (leader) {
+            for (int t = 0; t < nq; ++t) {
+                issue_s(qb, t, rk % C::kStages);
+                mma_commit(&c.bar.s_full[t]);
             }
-            if (leader) {
-                issue_s(qb, (g + t) & 1, rk % C::kStages);
-                mma_commit(&c.bar.s_full[(g + t) & 1]);
-                mma_commit(&c.bar.empty[rk % C::kStages]);
-                if (t == tiles - 1)
-                    mma_commit(&c.bar.q_empty[qb]);
-            }
-            __syncwarp();
+            mma_commit(&empty[rk % C::kStages]);
+            if (it.g.n_lo == it.g.n_hi)
+                mma_commit(&c.bar.q_empty[qb]);
         }
-        for (int t = 0; ok && t < tiles; ++t) {
-            const uint32_t gg = g + t, buf = gg & 1;
-            const uint32_t rv = base + 2 * t + 1;
-            const uint32_t vq = v_idx++;
-            uint64_t* vbar = FP8 ? &c.bar.full[rv % C::kStages] : &c.bar.vready[vq % (FP8 ? 1 : C::kVReady)];
-            const uint32_t vpar = FP8 ? (rv / C::kStages) & 1 : (vq / (FP8 ? 1 : C::kVReady)) & 1;
-            if (!wait_bar(vbar, vpar, c.abort_flag, p.err) ||
-                (t == 0 && n > 0 && !wait_bar(c.bar.o_empty, (n - 1) & 1, c.abort_flag, p.err)) ||
-                !wait_bar(&c.bar.p_full[buf], (gg >> 1) & 1, c.abort_flag, p.err)) {
+        __syncwarp();
+        for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
+            const bool last = j == it.g.n_hi;
+            const uint32_t rv = ring_idx++;
+            const uint32_t rk2 = last ? 0u : ring_idx++;
+            if (!wait_full(rv)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            if (leader) {
-                issue_pv(buf, rv % C::kStages, t > 0);
-                mma_commit(&c.bar.empty[rv % C::kStages]);
-                mma_commit(c.bar.pv_done);
-                if (t == tiles - 1)
-                    mma_commit(c.bar.o_full);
-            }
-            __syncwarp();
-            if (t + 2 < tiles) {
-                const uint32_t rk = base + 2 * (t + 2);
-                if (!wait_full(rk)) {
-                    ok = false;
-                    break;
+            if (!FP8) {
+                // keys >= kv_len: V rows may hold any bits (or a page that was not
+                // loaded); zero them so that P = 0 there cannot meet a NaN.
+                const int r0 = it.kv_len - j * kKvTile;
+                if (r0 < kKvTile) {
+                    uint8_t* vt = c.base + C::kOffRing + (rv % C::kStages) * C::kKvTileBytes;
+                    const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        uint4* dst = reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + r0 * 128);
+                        for (int q = lane; q < n16; q += 32)
+                            dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
+            }
+            for (int t = 0; ok && t < nq; ++t) {
+                for (int half = 0; half < 2; ++half) {
+                    if (!wait_bar(&c.bar.p_full[2 * t + half], p_cnt[t] & 1, c.abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (leader)
+                        issue_pv(t, half, rv % C::kStages, j > it.g.n_lo);
+                    __syncwarp();
+                }
+                if (!ok)
+                    break;
+                ++p_cnt[t];
                 if (leader) {
-                    issue_s(qb, buf, rk % C::kStages);
-                    mma_commit(&c.bar.s_full[buf]);
-                    mma_commit(&c.bar.empty[rk % C::kStages]);
-                    if (t + 2 == tiles - 1)
-                        mma_commit(&c.bar.q_empty[qb]);
+                    if (t == nq - 1)
+                        mma_commit(&empty[rv % C::kStages]);
+                    if (last)
+                        mma_commit(&c.bar.o_full[t]);
                 }
                 __syncwarp();
+                if (!last) {
+                    if (t == 0) {
+                        if (!wait_full(rk2)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (leader) {
+                        issue_s(qb, t, rk2 % C::kStages);
+                        mma_commit(&c.bar.s_full[t]);
+                        if (t == nq - 1) {
+                            mma_commit(&empty[rk2 % C::kStages]);
+                            if (j + 1 == it.g.n_hi)
+                                mma_commit(&c.bar.q_empty[qb]);
+                        }
+                    }
+                    __syncwarp();
+                }
             }
         }
-        g += tiles;
     }
     // every MMA this thread issued has completed once the drain barrier flips
     if (leader)
@@ -434,8 +412,8 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
 }
 
 // ---------------------------------------------------------------------------
-// Softmax / correction / epilogue: warps 4-11.  Thread (half h, row r) owns
-// keys 64h .. 64h+63 of row r of every S tile and O columns h*D/2 .. h*D/2+D/2-1.
+// Softmax / correction / epilogue for query tile t: warps 4+4t .. 7+4t, one
+// thread per TMEM lane (= MMA row).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {
@@ -445,35 +423,32 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
 }
 
 template <int D, bool FP8>
-__device__ void softmax_role(const AttnParams& p, const Ctx& c)
+__device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 {
     using C = TcCfg<D, FP8>;
     constexpr float kLog2e = 1.4426950408889634f;
-    constexpr int kHalfKeys = kKvTile / 2;  // 64 keys per thread
-    constexpr int kOCols = D / 2;           // O columns per thread
-    const int h = (threadIdx.x >> 7) - 1;   // 0: warps 4-7, 1: warps 8-11
     const int wq = (threadIdx.x >> 5) & 3;
     const int lane = threadIdx.x & 31;
     const int row = wq * 32 + lane;
-    const uint32_t tmem = __shfl_sync(0xffffffffu, c.tmem, 0);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t o_tmem = tmem + lane_off + (uint32_t)(C::kOCol + h * kOCols);
-    float* xmax = reinterpret_cast<float*>(c.base + C::kOffXchg);   // [2 tiles][2 halves][128]
-    float* xsum = xmax + 4 * kQRows;                                   // [2 halves][128]
+    const uint32_t s_tmem = c.tmem + lane_off + (uint32_t)(t * kKvTile);
+    const uint32_t o_tmem = c.tmem + lane_off + (uint32_t)(C::kOCol + t * D);
     const int G = p.G, Tq = p.rows_per_tile;
     const int r_tok = row / G, r_head = row % G;
     const bool row_real = row < G * Tq;
     const float sl2 = p.scale_log2;
 
-    uint32_t g = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
         const int w = take_item<C::kItemSlots>(p, c, n, &ok);
         if (w < 0)
             break;
         const ItemInfo it = read_item(p, w);
+        if (t >= it.g.nq)
+            continue;
         const int prefix = it.kv_len - it.q_len;
-        const int i_first = it.g.tok0;
+        const int i_first = it.g.tok0 + t * Tq;
         const int i = i_first + r_tok;
         const bool valid = row_real && i < it.q_len;
         const int pos = prefix + i;
@@ -485,58 +460,50 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c)
 
         float m_used = -INFINITY;
         float l = 0.f;
-        for (int j = it.g.n_lo; j <= it.g.n_hi; ++j, ++g) {
-            const uint32_t buf = g & 1;
-            const uint32_t s_tmem = tmem + lane_off + buf * (uint32_t)kKvTile;
-            bool tile_ok = wait_bar(&c.bar.s_full[buf], (g >> 1) & 1, c.abort_flag, p.err);
+        for (int j = it.g.n_lo; j <= it.g.n_hi; ++j) {
+            if (!wait_bar(&c.bar.s_full[t], s_cnt & 1, c.abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
+            ++s_cnt;
             tc_fence_after();
-            float s[kHalfKeys];
-            if (tile_ok) {
+            float s[kKvTile];
+            float mq[4];  // maxima of the four 32-key loads
+            {
                 uint32_t r[32];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    tmem_ld32(s_tmem + (uint32_t)(h * kHalfKeys + q * 32), r);
+                for (int q = 0; q < 4; ++q) {
+                    tmem_ld32_max(s_tmem + (uint32_t)(q * 32), r, &mq[q]);
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
                         s[q * 32 + k] = __uint_as_float(r[k]);
                 }
                 tmem_wait_ld();
+            }
+            const int k0 = j * kKvTile;
+            const bool interior = k0 >= lo_last && k0 + kKvTile - 1 <= p_first;
+            float mx;
+            if (interior) {
+                mx = fmax3(fmax3(mq[0], mq[1], mq[2]), mq[3], -INFINITY);
             } else {
 #pragma unroll
-                for (int k = 0; k < kHalfKeys; ++k)
-                    s[k] = -INFINITY;
-            }
-            const int k0 = j * kKvTile + h * kHalfKeys;
-            const bool interior = k0 >= lo_last && k0 + kHalfKeys - 1 <= p_first;
-            if (!interior) {
-#pragma unroll
-                for (int k = 0; k < kHalfKeys; ++k) {
+                for (int k = 0; k < kKvTile; ++k) {
                     const int key = k0 + k;
                     if (key < lo || key > hi)
                         s[k] = -INFINITY;
                 }
-            }
-            // maximum over this thread's 64 keys: four independent 3-input max chains
-            float pm[4];
+                // masked row maximum: eight independent 3-input max chains
+                float pm[8];
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                float m = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
+                for (int a = 0; a < 8; ++a) {
+                    float m = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
 #pragma unroll
-                for (int k = 3; k < 15; k += 2)
-                    m = fmax3(m, s[16 * a + k], s[16 * a + k + 1]);
-                pm[a] = fmaxf(m, s[16 * a + 15]);
+                    for (int k = 3; k < 15; k += 2)
+                        m = fmax3(m, s[16 * a + k], s[16 * a + k + 1]);
+                    pm[a] = fmaxf(m, s[16 * a + 15]);
+                }
+                mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
             }
-            const float mh = fmax3(fmax3(pm[0], pm[1], pm[2]), pm[3], -INFINITY);
-            // exchange with the other half of the row (double buffered by tile parity)
-            xmax[(buf * 2 + h) * kQRows + row] = mh;
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c.bar.xch[buf]);
-            if (!tile_ok || !wait_bar(&c.bar.xch[buf], (g >> 1) & 1, c.abort_flag, p.err)) {
-                ok = false;
-                break;
-            }
-            const float mx = fmaxf(mh, xmax[(buf * 2 + (h ^ 1)) * kQRows + row]);
             const float m_tile = mx * sl2;
             // keep a stale maximum until the row maximum grows by more than 2^8:
             // exact, since the denominator uses the same stale maximum
@@ -547,81 +514,77 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c)
                 l *= alpha;
                 m_used = m_tile;
             }
-            if (__any_sync(0xffffffffu, need) && j > it.g.n_lo) {
-                // O must hold this item's sum up to tile j-1 before it is rescaled
-                if (!wait_bar(c.bar.pv_done, (g - 1) & 1, c.abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float f = need ? alpha : 1.f;
-                const float2 ff = make_float2(f, f);
-#pragma unroll
-                for (int q = 0; q < kOCols / 16; ++q) {
-                    uint32_t o[16];
-                    tmem_ld16(o_tmem + (uint32_t)(q * 16), o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 16; k += 2) {
-                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), ff);
-                        o[k] = __float_as_uint(v.x);
-                        o[k + 1] = __float_as_uint(v.y);
-                    }
-                    tmem_st16(o_tmem + (uint32_t)(q * 16), o);
-                }
-            }
             const float neg = m_used == -INFINITY ? 0.f : -m_used;
             const float2 sc = make_float2(sl2, sl2), ng = make_float2(neg, neg);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
-            uint32_t pk[kHalfKeys / 2];
+            const bool rescale = __any_sync(0xffffffffu, need) && j > it.g.n_lo;
 #pragma unroll
-            for (int k = 0; k < kHalfKeys / 2; ++k) {
-                const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
-                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                acc[k & 3] = __fadd2_rn(acc[k & 3], e);
-                if (FP8) {
-                    uint32_t r;
-                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
-                    pk[k] = r;
-                } else {
-                    pk[k] = pack_bf16x2(e.x, e.y);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const int k = half * 32 + kk;
+                    const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
+                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
+                    if (FP8) {
+                        uint32_t r;
+                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
+                        pk[kk] = r;
+                    } else {
+                        pk[kk] = pack_bf16x2(e.x, e.y);
+                    }
                 }
+                if (half == 0 && rescale) {
+                    // O holds this item's sum up to tile j-1 (S(j) was issued after
+                    // PV(j-1)); rescale it before the first P V of tile j
+                    const float f = need ? alpha : 1.f;
+                    const float2 ff = make_float2(f, f);
+#pragma unroll
+                    for (int q = 0; q < D / 16; ++q) {
+                        uint32_t o[16];
+                        tmem_ld16(o_tmem + (uint32_t)(q * 16), o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; k += 2) {
+                            const float2 v =
+                                __fmul2_rn(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), ff);
+                            o[k] = __float_as_uint(v.x);
+                            o[k + 1] = __float_as_uint(v.y);
+                        }
+                        tmem_st16(o_tmem + (uint32_t)(q * 16), o);
+                    }
+                }
+                tmem_st32(s_tmem + (uint32_t)(half * 32), pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&c.bar.p_full[2 * t + half]);
             }
-            // P keys 64h .. 64h+63 -> columns 32h .. 32h+31 of the S buffer (both
-            // halves have read their S columns before the exchange barrier)
-            tmem_st32(s_tmem + (uint32_t)(h * 32), pk);
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a = __fadd2_rn(a01, a23);
             l += a.x + a.y;
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c.bar.p_full[buf]);
         }
         if (!ok)
             break;
-        // epilogue: out = bmm2_scale * O / (l_0 + l_1 + e^{sink - m})
-        xsum[h * kQRows + row] = l;
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(c.bar.xsum);
-        if (!wait_bar(c.bar.xsum, n & 1, c.abort_flag, p.err) || !wait_bar(c.bar.o_full, n & 1, c.abort_flag, p.err)) {
+        // epilogue: out = bmm2_scale * O / (l + e^{sink - m})
+        if (!wait_bar(&c.bar.o_full[t], o_cnt & 1, c.abort_flag, p.err)) {
             ok = false;
             break;
         }
+        ++o_cnt;
         tc_fence_after();
-        const int hq = it.kvh * G + r_head;
-        float total = l + xsum[(h ^ 1) * kQRows + row];
+        const int h = it.kvh * G + r_head;
+        float total = l;
         if (p.sinks != nullptr && m_used != -INFINITY && row_real)
-            total += ex2_approx(fmaf(p.sinks[hq], kLog2e, -m_used));
+            total += ex2_approx(fmaf(p.sinks[h], kLog2e, -m_used));
         const float inv = (m_used != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
         const float2 inv2 = make_float2(inv, inv);
-        uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok +
-                         (long long)hq * p.out_stride_head + h * kOCols;
+        uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
 #pragma unroll
-        for (int q = 0; q < kOCols / 32; ++q) {
+        for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
             tmem_wait_ld();
@@ -639,10 +602,6 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c)
                     dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(c.bar.o_empty);
     }
     tc_fence_before();
 }
@@ -684,8 +643,8 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
-        {
-            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + qb * C::kQTileBytes);
+        for (int t = 0; t < it.g.nq; ++t) {
+            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + (qb * kQTiles + t) * C::kQTileBytes);
             for (int k = ct; k < C::kQTileBytes / 16; k += 128) {
                 uint4 v = q[k];
                 v.x = bf16x2_to_f16x2(v.x);
@@ -757,18 +716,13 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     c.bar.empty = c.bar.full + C::kStages;
     c.bar.f8full = c.bar.empty + C::kStages;
     c.bar.f8empty = c.bar.f8full + C::kF8Stages;
-    c.bar.vready = c.bar.f8empty + C::kF8Stages;
-    c.bar.q_full = c.bar.vready + C::kVReady;
+    c.bar.q_full = c.bar.f8empty + C::kF8Stages;
     c.bar.q_empty = c.bar.q_full + C::kQBufs;
     c.bar.q_conv = c.bar.q_empty + C::kQBufs;
     c.bar.s_full = c.bar.q_conv + C::kQBufs;
-    c.bar.p_full = c.bar.s_full + 2;
-    c.bar.xch = c.bar.p_full + 2;
-    c.bar.xsum = c.bar.xch + 2;
-    c.bar.pv_done = c.bar.xsum + 1;
-    c.bar.o_full = c.bar.pv_done + 1;
-    c.bar.o_empty = c.bar.o_full + 1;
-    c.bar.drain = c.bar.o_empty + 1;
+    c.bar.p_full = c.bar.s_full + kQTiles;
+    c.bar.o_full = c.bar.p_full + 2 * kQTiles;
+    c.bar.drain = c.bar.o_full + kQTiles;
     c.bar.it_full = c.bar.drain + 1;
     c.bar.it_empty = c.bar.it_full + C::kItemSlots;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
@@ -785,22 +739,17 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             mbar_init(&c.bar.f8full[s], 1);
             mbar_init(&c.bar.f8empty[s], 4);
         }
-        for (int s = 0; s < C::kVReady; ++s)
-            mbar_init(&c.bar.vready[s], 1);
         for (int b = 0; b < C::kQBufs; ++b) {
             mbar_init(&c.bar.q_full[b], 1);
             mbar_init(&c.bar.q_empty[b], 1);
             mbar_init(&c.bar.q_conv[b], 4);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&c.bar.s_full[b], 1);
-            mbar_init(&c.bar.p_full[b], 8);
-            mbar_init(&c.bar.xch[b], 8);
+        for (int t = 0; t < kQTiles; ++t) {
+            mbar_init(&c.bar.s_full[t], 1);
+            mbar_init(&c.bar.p_full[2 * t], 4);
+            mbar_init(&c.bar.p_full[2 * t + 1], 4);
+            mbar_init(&c.bar.o_full[t], 1);
         }
-        mbar_init(c.bar.xsum, 8);
-        mbar_init(c.bar.pv_done, 1);
-        mbar_init(c.bar.o_full, 1);
-        mbar_init(c.bar.o_empty, 8);
         mbar_init(c.bar.drain, 1);
         for (int s = 0; s < C::kItemSlots; ++s) {
             mbar_init(&c.bar.it_full[s], 1);
@@ -824,7 +773,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         const int pad = C::kHalfBytes - used;
         if (pad > 0) {
             const int n16 = pad / 16;
-            for (int k = threadIdx.x; k < C::kQBufs * C::kHalves * n16; k += blockDim.x) {
+            for (int k = threadIdx.x; k < C::kQBufs * kQTiles * C::kHalves * n16; k += blockDim.x) {
                 const int blk = k / n16, q = k % n16;
                 *reinterpret_cast<uint4*>(base + C::kOffQ + blk * C::kHalfBytes + used + q * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
@@ -843,7 +792,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
 
     if constexpr (FP8) {
         // 512 threads launch with 128 registers each; the softmax warpgroups
-        // take registers from the others (64 + 160 + 160 + 128 = 512 = 4 x 128)
+        // take registers from the others (64 + 184 + 184 + 80 = 512 = 4 x 128)
         if (warp < 4) {
             regs_dec<64>();
             if (warp == 0)
@@ -851,20 +800,24 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             else if (warp == 1)
                 mma_role<D, FP8>(p, c);
         } else if (warp < 12) {
-            regs_inc<160>();
-            softmax_role<D, FP8>(p, c);
+            regs_inc<184>();
+            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
         } else {
+            regs_dec<80>();
             convert_role<D, FP8>(p, c);
         }
     } else {
-        if (warp == 0)
-            producer_role<D, FP8>(p, c);
-        else if (warp == 1)
-            mma_role<D, FP8>(p, c);
-        else if (warp == 2)
-            vrelease_role<D, FP8>(p, c);
-        else if (warp >= 4)
-            softmax_role<D, FP8>(p, c);
+        // 384 threads launch with 168 registers each (64 + 216 + 216 = 496 <= 3 x 168)
+        if (warp < 4) {
+            regs_dec<64>();
+            if (warp == 0)
+                producer_role<D, FP8>(p, c);
+            else if (warp == 1)
+                mma_role<D, FP8>(p, c);
+        } else {
+            regs_inc<216>();
+            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+        }
     }
 
     tc_fence_before();

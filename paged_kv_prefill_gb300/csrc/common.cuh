@@ -12,7 +12,7 @@ namespace b2pa {
 
 constexpr int kKvTile = 128;      // keys per kv tile (MMA N of Q K^T, K of P V)
 constexpr int kQRows = 128;       // MMA M rows per query tile (tokens x heads of one kv group)
-constexpr int kQTiles = 1;        // query tiles per work item
+constexpr int kQTiles = 2;        // query tiles per work item (they share every K/V tile)
 constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
