@@ -29,9 +29,9 @@
 //                 layout, and the Q tile from bf16 to f16.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
-// P_t (16-bit, two per column) overwrites the first 64 columns of S_t; it is
-// handed to the MMA warp in two halves (keys 0-63, 64-127) so that P V on the
-// first half overlaps the softmax of the second.
+// P_t (16-bit, two per column) overwrites the first 64 columns of S_t and is
+// handed to the MMA warp in kPParts parts (one: each extra hand-off costs the
+// MMA warp more than the overlap gains).
 //
 // The row maximum of an S tile comes with its TMEM load (tcgen05.ld.red, an
 // sm_103a instruction) except on tiles that need masking.
@@ -65,7 +65,9 @@ struct TcCfg {
     static constexpr int kOffRing = kOffQ + kQBufs * kQTiles * kQTileBytes;
     static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
     static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 * kQBufs + 4 * kQTiles + 1 + 2 * kItemSlots;
+    // P_t is handed to the MMA warp in kPParts parts of kKvTile / kPParts keys
+    static constexpr int kPParts = 1;
+    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
@@ -83,7 +85,7 @@ struct Bars {
     uint64_t* q_empty;   // [kQBufs]   last Q K^T of the item done
     uint64_t* q_conv;    // [kQBufs]   (FP8) Q converted to f16
     uint64_t* s_full;    // [2]        S_t in TMEM
-    uint64_t* p_full;    // [2][2]     half h of P_t in TMEM (4 softmax warps)
+    uint64_t* p_full;    // [2][kPParts] part h of P_t in TMEM (4 softmax warps)
     uint64_t* o_full;    // [2]        last P V of the item done
     uint64_t* drain;
     uint64_t* it_full;   // [kItemSlots] item index posted
@@ -295,14 +297,15 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
             mma_ss_w(d, a0 + off, b0 + off, kHi, kIdescS, k > 0 ? 1u : 0u);
         }
     };
-    // P V over keys 64 * half .. 64 * half + 63
-    auto issue_pv = [&](int t, int half, uint32_t slot, bool acc) {
+    // P V over the keys of part `part` of the tile
+    auto issue_pv = [&](int t, int part, uint32_t slot, bool acc) {
+        constexpr int kSteps = kKvTile / 16 / C::kPParts;
         const uint32_t b0 = v_lo + slot * kStageW;
         const uint32_t d = c.tmem + (uint32_t)(C::kOCol + t * D);
         const uint32_t a = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
-        for (int kk = 0; kk < kKvTile / 32; ++kk) {
-            const int k = half * (kKvTile / 32) + kk;                  // 16 keys = 16 rows of 128 B
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const int k = part * kSteps + kk;                          // 16 keys = 16 rows of 128 B
             mma_ts_w(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
         }
     };
@@ -363,14 +366,14 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 }
             }
             for (int t = 0; ok && t < nq; ++t) {
-                for (int half = 0; half < 2; ++half) {
-                    if (!wait_bar(&c.bar.p_full[2 * t + half], p_cnt[t] & 1, c.abort_flag, p.err)) {
+                for (int part = 0; part < C::kPParts; ++part) {
+                    if (!wait_bar(&c.bar.p_full[C::kPParts * t + part], p_cnt[t] & 1, c.abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (leader)
-                        issue_pv(t, half, rv % C::kStages, j > it.g.n_lo);
+                        issue_pv(t, part, rv % C::kStages, j > it.g.n_lo);
                     __syncwarp();
                 }
                 if (!ok)
@@ -519,24 +522,31 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                              make_float2(0.f, 0.f)};
             const bool rescale = __any_sync(0xffffffffu, need) && j > it.g.n_lo;
+            // P in kPParts parts (two keys per column, part h in columns
+            // h * 64 / kPParts ..), each stored 16 columns at a time as produced
+            constexpr int kPartPairs = kKvTile / 2 / C::kPParts;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
+            for (int part = 0; part < C::kPParts; ++part) {
 #pragma unroll
-                for (int kk = 0; kk < 32; ++kk) {
-                    const int k = half * 32 + kk;
-                    const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
-                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                    acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
-                    if (FP8) {
-                        uint32_t r;
-                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
-                        pk[kk] = r;
-                    } else {
-                        pk[kk] = pack_bf16x2(e.x, e.y);
+                for (int q = 0; q < kPartPairs / 16; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const int k = part * kPartPairs + q * 16 + kk;
+                        const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
+                        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
+                        if (FP8) {
+                            uint32_t r;
+                            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
+                            pk[kk] = r;
+                        } else {
+                            pk[kk] = pack_bf16x2(e.x, e.y);
+                        }
                     }
+                    tmem_st16(s_tmem + (uint32_t)(part * kPartPairs + q * 16), pk);
                 }
-                if (half == 0 && rescale) {
+                if (part == 0 && rescale) {
                     // O holds this item's sum up to tile j-1 (S(j) was issued after
                     // PV(j-1)); rescale it before the first P V of tile j
                     const float f = need ? alpha : 1.f;
@@ -556,12 +566,11 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                         tmem_st16(o_tmem + (uint32_t)(q * 16), o);
                     }
                 }
-                tmem_st32(s_tmem + (uint32_t)(half * 32), pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&c.bar.p_full[2 * t + half]);
+                    mbar_arrive(&c.bar.p_full[C::kPParts * t + part]);
             }
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a = __fadd2_rn(a01, a23);
@@ -721,7 +730,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     c.bar.q_conv = c.bar.q_empty + C::kQBufs;
     c.bar.s_full = c.bar.q_conv + C::kQBufs;
     c.bar.p_full = c.bar.s_full + kQTiles;
-    c.bar.o_full = c.bar.p_full + 2 * kQTiles;
+    c.bar.o_full = c.bar.p_full + C::kPParts * kQTiles;
     c.bar.drain = c.bar.o_full + kQTiles;
     c.bar.it_full = c.bar.drain + 1;
     c.bar.it_empty = c.bar.it_full + C::kItemSlots;
@@ -746,8 +755,8 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         }
         for (int t = 0; t < kQTiles; ++t) {
             mbar_init(&c.bar.s_full[t], 1);
-            mbar_init(&c.bar.p_full[2 * t], 4);
-            mbar_init(&c.bar.p_full[2 * t + 1], 4);
+            for (int h = 0; h < C::kPParts; ++h)
+                mbar_init(&c.bar.p_full[C::kPParts * t + h], 4);
             mbar_init(&c.bar.o_full[t], 1);
         }
         mbar_init(c.bar.drain, 1);
