@@ -142,6 +142,49 @@ B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_p
                            b2pa_stream_t stream);
 
 /*
+ * b2pa_context_attention_noalloc -- the same attention, for callers that must
+ * not have the library allocate GPU memory.  The pages describe no such entry
+ * point; it is an addition of this library.
+ *
+ * Who needs it: a serving engine that reserves nearly all of HBM for its KV
+ * pool at start-up, and a framework whose own allocator accounts for every
+ * byte, cannot let a library call cudaMalloc behind its back: the call could
+ * fail once memory is taken, or break the caller's budget.
+ * b2pa_context_attention grows a per-stream workspace with cudaMalloc on
+ * first use; this entry point calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Its scratch (error word, work counter and the scheduler's work list) is a
+ * fixed array inside the library: 256 B + 65536 work items x 16 B = 1 MiB +
+ * 256 B, held on every GPU that loads the library until the process exits.
+ * A call whose bounds need more than 65536 work items (batch x kv heads x
+ * ceil(max_q_len / (2 * 128 / (H / Hkv)))) is rejected with
+ * B2PA_ERR_INVALID_ARG and a message saying so; use b2pa_context_attention
+ * for those.
+ *
+ * Arguments and results are those of b2pa_context_attention, plus:
+ *  dev_status    NULL, or a caller-owned device uint32 that receives this
+ *                call's device error word (b2pa_device_error bits) in stream
+ *                order.  b2pa_get_device_status does not see this entry
+ *                point's errors.
+ * Only the tensor-core path runs here: a shape it cannot take returns
+ * B2PA_ERR_UNSUPPORTED (b2pa_query_path tells beforehand).
+ *
+ * The first call on a device looks up the scratch's device address there
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's contents; the call clears the error word itself.  Calls whose
+ * kernels overlap on the GPU (on different streams, or from different host
+ * threads) race on the scratch and give undefined results: serialise them.
+ */
+B2PA_API int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_tensor* k_pool,
+                           const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
+                           const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q, const b2pa_tensor* cum_kv,
+                           int32_t max_q_len, int32_t max_kv_len, float bmm1_scale, float bmm2_scale,
+                           int32_t window_left, const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out,
+                           uint32_t* dev_status, b2pa_stream_t stream);
+
+/*
  * b2pa_debug_worklist -- run only the scheduler of the tensor-core path and
  * copy its work list to the host (synchronises `stream`).
  *

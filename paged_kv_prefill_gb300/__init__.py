@@ -39,6 +39,7 @@ _DTYPES = {
 
 EXPORTED = [
     "b2pa_context_attention",
+    "b2pa_context_attention_noalloc",
     "b2pa_debug_worklist",
     "b2pa_debug_gather",
     "b2pa_get_device_status",
@@ -83,6 +84,10 @@ def load(path: str = LIB_PATH):
     lib.b2pa_context_attention.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                            ctypes.c_float, ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
     lib.b2pa_context_attention.restype = ctypes.c_int
+    lib.b2pa_context_attention_noalloc.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                                   ctypes.c_float, ctypes.c_float, ctypes.c_int32, P,
+                                                   ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_void_p]
+    lib.b2pa_context_attention_noalloc.restype = ctypes.c_int
     lib.b2pa_debug_worklist.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p]
@@ -189,6 +194,46 @@ def context_attention(
         int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
     )
     _check(st, "b2pa_context_attention")
+    return out
+
+
+def context_attention_noalloc(
+    query: torch.Tensor,
+    kv_cache: Union[torch.Tensor, Sequence[torch.Tensor]],
+    block_tables: torch.Tensor,
+    seq_lens: torch.Tensor,
+    max_q_len: int,
+    max_kv_len: int,
+    bmm1_scale: float,
+    bmm2_scale: float,
+    cum_seq_lens_q: torch.Tensor,
+    out: torch.Tensor,
+    cum_seq_lens_kv: Optional[torch.Tensor] = None,
+    window_left: int = -1,
+    kv_layout: str = "HND",
+    sinks: Optional[torch.Tensor] = None,
+    status: Optional[torch.Tensor] = None,
+    stream=None,
+) -> torch.Tensor:
+    """context_attention through b2pa_context_attention_noalloc: the library
+    allocates no GPU memory (its scratch is a fixed array of 65536 work items;
+    see include/b2pa.h).  `out` must be given; `status`, if given, is a device
+    int32/uint32 tensor of one element that receives the call's device error bits."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    if isinstance(sinks, (list, tuple)):
+        if len(sinks) != 1:
+            raise ValueError("sinks: one fp32 [num_heads] tensor")
+        sinks = sinks[0]
+    dq, dk, dv, dbt, dsl, dcq = (desc(x) for x in (query, k, v, block_tables, seq_lens, cum_seq_lens_q))
+    dck, dsk, do = desc(cum_seq_lens_kv), desc(sinks), desc(out)
+    st = lib.b2pa_context_attention_noalloc(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dbt), ctypes.byref(dsl),
+        ctypes.byref(dcq), _ref(dck), int(max_q_len), int(max_kv_len), float(bmm1_scale), float(bmm2_scale),
+        int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do),
+        ctypes.c_void_p(status.data_ptr() if status is not None else 0), ctypes.c_void_p(_stream_handle(stream)),
+    )
+    _check(st, "b2pa_context_attention_noalloc")
     return out
 
 

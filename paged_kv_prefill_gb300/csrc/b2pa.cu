@@ -798,3 +798,136 @@ void b2pa_release(void)
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free entry point
+//
+// b2pa_context_attention_noalloc runs the same scheduler and tensor-core
+// attention kernels as b2pa_context_attention, but the scratch they need (the
+// error word, the work counter, the item count and the work list) lives in the
+// fixed array below instead of a cudaMalloc'd per-stream workspace.
+
+namespace {
+
+constexpr size_t kNoAllocItems = 65536;                                 // work items at most
+constexpr size_t kNoAllocBytes = kWsHeader + kNoAllocItems * sizeof(int4);  // 1 MiB + 256 B
+
+}  // namespace
+
+// Shared by every call of the allocation-free entry point on a device; each
+// GPU that loads this library holds one copy until the process exits.  Host
+// code must not use this name as an address: it resolves it per device with
+// cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+uint8_t* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per device ordinal
+
+// Device address of the scratch on device `dev` (which must be current);
+// looked up once per device.
+int noalloc_scratch(int dev, uint8_t** out)
+{
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(allocation-free scratch)");
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return B2PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                                   const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens,
+                                   const b2pa_tensor* cum_q, const b2pa_tensor* cum_kv, int32_t max_q_len,
+                                   int32_t max_kv_len, float bmm1_scale, float bmm2_scale, int32_t window_left,
+                                   const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out,
+                                   uint32_t* dev_status, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    Problem pr;
+    int st = parse_problem(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, sinks, layout, out, &pr);
+    if (st)
+        return st;
+    if (max_q_len < 0 || max_kv_len < 0)
+        return fail(B2PA_ERR_INVALID_ARG, "max_q_len / max_kv_len must be >= 0");
+    if (!std::isfinite(bmm1_scale) || !(bmm1_scale > 0.f) || !std::isfinite(bmm2_scale))
+        return fail(B2PA_ERR_INVALID_ARG, "bmm1_scale must be finite and > 0, bmm2_scale finite");
+    const size_t cap = items_needed(pr, max_q_len);
+    if (cap > kNoAllocItems)
+        return fail(B2PA_ERR_INVALID_ARG,
+                    "these bounds need %zu work items; the allocation-free entry point holds at most %zu "
+                    "(batch x kv heads x ceil(max_q_len / (2 x 128 / group size))); use b2pa_context_attention",
+                    cap, kNoAllocItems);
+    if (pr.B == 0 || pr.T == 0) {
+        if (dev_status) {
+            cudaError_t e = cudaMemsetAsync(dev_status, 0, sizeof(uint32_t), stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMemsetAsync(dev_status)");
+        }
+        return B2PA_OK;
+    }
+    int dev;
+    DevInfo di;
+    if ((st = device_info(&dev, &di)))
+        return st;
+    if (const char* why = tc_reject(pr, di))
+        return fail(B2PA_ERR_UNSUPPORTED, "the allocation-free entry point runs the tensor-core path only: %s", why);
+    uint8_t* mem = nullptr;
+    if ((st = noalloc_scratch(dev, &mem)))
+        return st;
+    const Workspace ws{dev, stream, mem, kNoAllocBytes};
+
+    AttnParams ap;
+    std::memset(&ap, 0, sizeof ap);
+    const int rpt = rows_per_tile_of(pr);
+    if ((st = encode_q_map(&ap.tm_q, pr, rpt)) || (st = encode_pool_map(&ap.tm_k, pr, pr.k, pr.k_st)) ||
+        (st = encode_pool_map(&ap.tm_v, pr, pr.v, pr.v_st)))
+        return st;
+    // the error word must start at zero (the scheduler resets the work counter itself)
+    cudaError_t e = cudaMemsetAsync(mem, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(error word)");
+    const int window = window_left < 0 ? -1 : window_left;
+    SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
+    if ((e = launch_schedule(sp, stream)) != cudaSuccess)
+        return cuda_fail(e, "scheduler launch");
+    ap.cum_q = pr.cum_q;
+    ap.seq_lens = pr.seq;
+    ap.block_tables = pr.bt;
+    ap.sinks = pr.sinks;
+    ap.out = static_cast<uint16_t*>(pr.out);
+    ap.bt_stride = pr.bt_stride;
+    ap.out_stride_tok = pr.out_st_tok;
+    ap.out_stride_head = pr.out_st_head;
+    ap.items = sp.items;
+    ap.count = sp.count;
+    ap.counter = sp.counter;
+    ap.err = sp.err;
+    ap.cap = (int)cap;
+    ap.H = pr.H;
+    ap.Hkv = pr.Hkv;
+    ap.G = pr.H / pr.Hkv;
+    ap.rows_per_tile = rpt;
+    ap.page_size = pr.P;
+    ap.num_pages = pr.N;
+    ap.window = window;
+    ap.scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
+    ap.bmm2 = bmm2_scale;
+    if ((e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true)) != cudaSuccess)
+        return cuda_fail(e, "attention kernel launch");
+    if (dev_status && (e = cudaMemcpyAsync(dev_status, mem, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream)) !=
+                          cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(dev_status)");
+    return B2PA_OK;
+}
+
+}  // extern "C"
