@@ -420,6 +420,10 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     sp.num_pages = pr.N;
     sp.debug = g_debug.load();
     sp.cap = (int)cap;
+    // an item touches at most ceil(max_kv_len / kKvTile) kv tiles of each of its
+    // query tiles; with that many buckets no cost is capped below kCostCap
+    const long long max_cost = (long long)((max_kv_len + kKvTile - 1) / kKvTile) * kQTiles;
+    sp.nbuckets = (int)(max_cost + 1 < kSchedBuckets ? (max_cost + 1 > 2 ? max_cost + 1 : 2) : kSchedBuckets);
     sp.items = reinterpret_cast<int4*>(ws.mem + kWsHeader);
     sp.count = reinterpret_cast<int*>(ws.mem + 4);
     sp.counter = reinterpret_cast<int*>(ws.mem + 8);

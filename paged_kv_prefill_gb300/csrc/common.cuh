@@ -77,6 +77,7 @@ struct SchedParams {
     int B, Hkv, rows_per_tile, window, max_q_len, max_kv_len, page_size, max_pages, num_tokens, num_pages;
     int debug;
     int cap;
+    int nbuckets;             // cost buckets in use: min(kSchedBuckets, largest possible cost + 1)
     int4* items;
     int* count;
     int* counter;             // work counter of the attention kernel, reset here

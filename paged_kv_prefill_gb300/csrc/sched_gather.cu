@@ -12,7 +12,9 @@ namespace b2pa {
 //    Hkv * ceil(q_len / (rows_per_tile * kQTiles)).
 // 2. Enumerate items in (b, kv head, it) order; cost = kv tiles x non-empty
 //    query tiles (item_geometry), bucket = min(cost, kCostCap).
-// 3. Stable counting sort by bucket, descending: each warp owns a contiguous
+// 3. Stable counting sort by bucket, descending (p.nbuckets buckets: as many as
+//    the largest possible cost needs, so bucket = cost unless the cost reaches
+//    kCostCap): each warp owns a contiguous
 //    slice of the enumeration, counts per bucket with __match_any_sync,
 //    bucket starts come from a scan over (bucket descending, warp ascending),
 //    and a second pass scatters each item to its rank.  The order is fully
@@ -96,8 +98,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             }
         }
     }
-    for (int k = tid; k < 32 * kSchedBuckets; k += kSchedThreads)
-        hist[k] = 0;
+    const int nb = p.nbuckets;
+    for (int k = tid; k < 32 * nb; k += kSchedThreads)
+        hist[(k / nb) * kSchedBuckets + k % nb] = 0;
     int n_total = 0;
     int run = block_exclusive_scan(local, scratch, &n_total);
     for (int b = b_begin; b < b_end; ++b) {
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         const ItemGeom g = item_geometry(q_len, kv_len, it, p.rows_per_tile, p.window);
         const int cost = (g.n_hi - g.n_lo + 1) * g.nq;
         item = make_int4(b, kvh, it, cost);
-        bucket = min(cost, kCostCap);
+        bucket = min(cost, nb - 1);
     };
 
     const int seg = (n_total + 31) / 32;
@@ -153,8 +156,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     __syncthreads();
 
     // 3. offsets: buckets in descending order, warps in ascending order
-    {
-        const int c = tid;  // kSchedBuckets == kSchedThreads
+    if (tid < nb) {
+        const int c = tid;  // nb <= kSchedBuckets == kSchedThreads
         int acc = 0;
         for (int w = 0; w < 32; ++w) {
             const int v = hist[w * kSchedBuckets + c];
@@ -164,10 +167,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         tot[c] = acc;
     }
     __syncthreads();
-    // exclusive scan over buckets from the top: thread t takes bucket kCostCap - t
-    const int start = block_exclusive_scan(tot[kCostCap - tid], scratch, nullptr);
-    {
-        const int c = kCostCap - tid;
+    // exclusive scan over buckets from the top: thread t takes bucket nb - 1 - t
+    const int start = block_exclusive_scan(tid < nb ? tot[nb - 1 - tid] : 0, scratch, nullptr);
+    if (tid < nb) {
+        const int c = nb - 1 - tid;
         for (int w = 0; w < 32; ++w)
             hist[w * kSchedBuckets + c] += start;
     }
