@@ -530,18 +530,27 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 #pragma unroll
                 for (int q = 0; q < kPartPairs / 16; ++q) {
                     uint32_t pk[16];
+                    // on a masked tile, 32 keys that no row of this warp sees give P = 0
+                    // without any exponential
+                    const int c0 = k0 + 2 * (part * kPartPairs + q * 16);
+                    if (!interior && __all_sync(0xffffffffu, c0 > hi || c0 + 31 < lo)) {
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const int k = part * kPartPairs + q * 16 + kk;
-                        const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
-                        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
-                        if (FP8) {
-                            uint32_t r;
-                            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
-                            pk[kk] = r;
-                        } else {
-                            pk[kk] = pack_bf16x2(e.x, e.y);
+                        for (int kk = 0; kk < 16; ++kk)
+                            pk[kk] = 0u;
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const int k = part * kPartPairs + q * 16 + kk;
+                            const float2 x = __ffma2_rn(make_float2(s[2 * k], s[2 * k + 1]), sc, ng);
+                            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            acc[kk & 3] = __fadd2_rn(acc[kk & 3], e);
+                            if (FP8) {
+                                uint32_t r;
+                                asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(e.y), "f"(e.x));
+                                pk[kk] = r;
+                            } else {
+                                pk[kk] = pack_bf16x2(e.x, e.y);
+                            }
                         }
                     }
                     tmem_st16(s_tmem + (uint32_t)(part * kPartPairs + q * 16), pk);
