@@ -254,6 +254,56 @@ def time_oracle(inp, rows):
 
 # --------------------------------------------------------------------------- our arm
 
+def run_all_workloads(reps: int = 20):
+    """One JSON line per named workload (not the bench contract line): median
+    device time of the attention kernel alone and of the whole call, each
+    after a 512 MiB L2 flush, with effective TFLOP/s and algorithmic GB/s."""
+    import paged_kv_prefill_gb300 as b2pa
+    from paged_kv_prefill_gb300 import build as b2pa_build
+
+    b2pa_build.build()
+    b2pa.load()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for idx, W in [(2, None), (3, None), (4, None), (4, -1), (5, None)]:
+        inp = workload.config(idx, window_left=W)
+        d = {n: getattr(inp, n).to(dev) for n in ("q", "k_pool", "v_pool", "block_tables", "seq_lens", "cum_q",
+                                                  "cum_kv")}
+        sinks = None if inp.sinks is None else inp.sinks.to(dev)
+        out = torch.empty_like(d["q"])
+
+        def call():
+            b2pa.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                   inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"],
+                                   d["cum_kv"], inp.window_left, out, inp.layout, sinks, stream=stream)
+
+        for _ in range(5):
+            call()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps)] for _ in range(4)]
+        for e in ev[0] + ev[1]:
+            e.record(stream)  # the CUDA event exists once recorded
+        torch.cuda.synchronize()
+        for i in range(reps):
+            flush.fill_(i)
+            b2pa.set_timing_events(ev[0][i], ev[1][i])
+            call()
+            b2pa.set_timing_events(None, None)
+            flush.fill_(i + 1)
+            ev[2][i].record(stream)
+            call()
+            ev[3][i].record(stream)
+        torch.cuda.synchronize()
+        k_ms = statistics.median(a.elapsed_time(b) for a, b in zip(ev[0], ev[1]))
+        c_ms = statistics.median(a.elapsed_time(b) for a, b in zip(ev[2], ev[3]))
+        fl, by = step_flops(inp), algorithmic_bytes(inp)
+        print(json.dumps({"workload": inp.name, "path": b2pa.query_path(d["q"], (d["k_pool"], d["v_pool"]), out,
+                                                                        inp.layout),
+                          "gflop": fl / 1e9, "algorithmic_mb": by / 1e6, "kernel_ms": k_ms, "call_ms": c_ms,
+                          "kernel_tflops": fl / k_ms / 1e9, "call_tflops": fl / c_ms / 1e9,
+                          "kernel_gbs": by / k_ms / 1e6, "device_status": b2pa.device_status()}), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import paged_kv_prefill_gb300 as b2pa
     from paged_kv_prefill_gb300 import build as b2pa_build
@@ -519,11 +569,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-fraction", type=float, default=0.125)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="time every named workload (kernel and call) instead of the bench line")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K calls of the workload (for ncu); prints no measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.all_workloads:
+        run_all_workloads()
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
