@@ -93,6 +93,44 @@ def test_tcgen05_parity_small(cuda_lib, case):
     _compare(out, inp)
 
 
+# the tensor-core path's limits: the largest kv-head group (one token per 128-row
+# query tile) and a wide group at D = 64
+LIMIT_CASES = [
+    ([40, 3], [300, 3], 128, 1, 128, 32, "HND", -1, True, "bf16"),   # G = 128
+    ([50, 20], [90, 200], 64, 2, 64, 16, "NHD", 60, False, "bf16"),  # G = 32, window
+]
+
+
+@pytest.mark.parametrize("case", range(len(LIMIT_CASES)))
+def test_tcgen05_group_size_limits(cuda_lib, case):
+    ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = LIMIT_CASES[case]
+    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=700 + case,
+                         table_pad="garbage")
+    out, bits = _run(cuda_lib, inp, "tcgen05")
+    assert bits == 0
+    _compare(out, inp)
+
+
+def test_scheduler_batch_limit(cuda_lib):
+    """4096 requests (the most the scheduler takes) on the tensor-core path, and
+    one more: the tensor-core path then refuses it and the automatic choice
+    computes it on the generic path."""
+    g = torch.Generator().manual_seed(77)
+    B = 4096
+    ql = torch.randint(0, 3, (B,), generator=g).tolist()
+    kl = [q + x for q, x in zip(ql, torch.randint(0, 40, (B,), generator=g).tolist())]
+    inp = workload.build(ql, kl, 8, 2, 128, 16, "HND", seed=78)
+    out, bits = _run(cuda_lib, inp, "tcgen05")
+    assert bits == 0
+    _compare(out, inp)
+    inp2 = workload.build(ql + [2], kl + [5], 8, 2, 128, 16, "HND", seed=79)
+    with pytest.raises(cuda_lib.B2paError, match="batch"):
+        _run(cuda_lib, inp2, "tcgen05")
+    out2, bits2 = _run(cuda_lib, inp2, "auto")
+    assert bits2 == 0
+    _compare(out2, inp2)
+
+
 @pytest.mark.parametrize("case", range(len(TC_CASES)))
 def test_generic_parity_small(cuda_lib, case):
     ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = TC_CASES[case]
