@@ -16,7 +16,10 @@
 //   warp 0        producer: item fetch; TMA loads of Q (3-D map, double
 //                 buffered across items where shared memory allows) and of
 //                 K/V pages (4-D map, one box per page and 128-byte column
-//                 block) through a ring of stages with full/empty mbarriers.
+//                 block) through a ring that holds K and V of a kv tile side
+//                 by side under one full and one empty mbarrier (FP8: the
+//                 converters signal K and V separately), so each tile costs
+//                 the MMA warp one wait and one release.
 //   warp 1        MMA issuer (one lane): S_t = Q_t K^T into TMEM, then
 //                 O_t += P_t V with P_t read from TMEM, for t = 0, 1, in the
 //                 order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) so the tensor
@@ -50,10 +53,12 @@ struct TcCfg {
     static constexpr int kHalfBytes = kQRows * 128;   // one column block of a 128-row tile
     static constexpr int kQTileBytes = kHalves * kHalfBytes;
     static constexpr int kKvTileBytes = kHalves * kHalfBytes;
-    // A kv tile j is in use from S(j) to PV(j); the ring must also hold the
-    // next K and V in flight: at least 4 stages, 5 where shared memory allows.
+    // The 16-bit K/V ring holds K and V of a kv tile side by side (entries 2m
+    // and 2m + 1) under one full and one empty barrier: a tile is in use from
+    // S(j) to P V(j), and the next tile lands meanwhile.
     static constexpr int kQBufs = D == 128 ? 1 : 2;                 // Q buffers (items in flight)
-    static constexpr int kStages = D == 128 ? (FP8 ? 4 : 5) : 8;    // 16-bit K/V ring
+    static constexpr int kStages = D == 128 ? 4 : 8;                // 16-bit ring entries
+    static constexpr int kPairs = kStages / 2;                      // tiles in the ring
     static constexpr int kF8Stages = FP8 ? 2 : 0;                   // e4m3 staging ring
     static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
     static constexpr int kThreads = FP8 ? 512 : 384;
@@ -67,7 +72,7 @@ struct TcCfg {
     static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
     // P_t is handed to the MMA warp in kPParts parts of kKvTile / kPParts keys
     static constexpr int kPParts = 1;
-    static constexpr int kNumBars = 2 * kStages + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
+    static constexpr int kNumBars = (FP8 ? 3 : 2) * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
@@ -77,8 +82,9 @@ struct TcCfg {
 };
 
 struct Bars {
-    uint64_t* full;      // [kStages]  16-bit K/V tile landed (TMA bytes, or converter warps)
-    uint64_t* empty;     // [kStages]  tile consumed by the MMAs
+    uint64_t* full;      // [kPairs]   16-bit K and V of a kv tile landed (TMA bytes, or converter warps)
+    uint64_t* empty;     // [kPairs]   K and V of the tile consumed by the MMAs
+    uint64_t* vfull;     // [kPairs]   (FP8) V of the tile converted; full then means K alone
     uint64_t* f8full;    // [kF8Stages]
     uint64_t* f8empty;   // [kF8Stages]
     uint64_t* q_full;    // [kQBufs]   Q tiles landed
@@ -230,31 +236,57 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
             const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
             const uint32_t bytes = nvalid * (uint32_t)box_rows * 128u * kBoxes;
-            for (int kind = 0; kind < 2; ++kind) {
-                const uint32_t s = ring_idx % kRingStages, ph = (ring_idx / kRingStages) & 1;
-                if (!wait_bar(&rempty[s], ph ^ 1, c.abort_flag, p.err)) {
+            if constexpr (!FP8) {
+                // K and V of the tile into one ring pair, under one barrier
+                const uint32_t m = ring_idx % C::kPairs, ph = (ring_idx / C::kPairs) & 1;
+                if (!wait_bar(&c.bar.empty[m], ph ^ 1, c.abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&rfull[s], bytes);
+                    mbar_arrive_expect_tx(&c.bar.full[m], 2 * bytes);
                 __syncwarp();
                 if (valid) {
-                    const uint32_t dst = ring + s * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
 #pragma unroll
-                    for (int h = 0; h < kBoxes; ++h)
-                        tma_load_4d(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &rfull[s], h * 64, slot0,
-                                    it.kvh, page);
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const uint32_t dst =
+                            ring + (2 * m + kind) * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
+#pragma unroll
+                        for (int h = 0; h < kBoxes; ++h)
+                            tma_load_4d(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &c.bar.full[m], h * 64,
+                                        slot0, it.kvh, page);
+                    }
                 }
                 ++ring_idx;
+            } else {
+                for (int kind = 0; kind < 2; ++kind) {
+                    const uint32_t s = ring_idx % kRingStages, ph = (ring_idx / kRingStages) & 1;
+                    if (!wait_bar(&rempty[s], ph ^ 1, c.abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&rfull[s], bytes);
+                    __syncwarp();
+                    if (valid) {
+                        const uint32_t dst = ring + s * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
+#pragma unroll
+                        for (int h = 0; h < kBoxes; ++h)
+                            tma_load_4d(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &rfull[s], h * 64, slot0,
+                                        it.kvh, page);
+                    }
+                    ++ring_idx;
+                }
             }
         }
     }
     if (*c.abort_flag) {
         // let the copies this warp started land before the CTA releases its memory
-        const uint32_t first = ring_idx > (uint32_t)kRingStages ? ring_idx - kRingStages : 0;
+        // (16-bit KV: ring_idx counts tiles, one barrier per pair; FP8: e4m3 entries)
+        constexpr int kSlots = FP8 ? kRingStages : C::kPairs;
+        const uint32_t first = ring_idx > (uint32_t)kSlots ? ring_idx - kSlots : 0;
         for (uint32_t k = first; k < ring_idx; ++k)
-            drain_wait(&rfull[k % kRingStages], (k / kRingStages) & 1);
+            drain_wait(&rfull[k % kSlots], (k / kSlots) & 1);
     }
 }
 
@@ -309,9 +341,12 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
             mma_ts_w(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
         }
     };
+    // ring pair r % kPairs holds K (entry 2m) and V (entry 2m + 1) of the r-th tile
     auto wait_full = [&](uint32_t r) -> bool {
-        return wait_bar(&full[r % C::kStages], (r / C::kStages) & 1, c.abort_flag, p.err);
+        return wait_bar(&full[r % C::kPairs], (r / C::kPairs) & 1, c.abort_flag, p.err);
     };
+    auto k_slot = [](uint32_t r) { return 2u * (r % C::kPairs); };
+    auto v_slot = [](uint32_t r) { return 2u * (r % C::kPairs) + 1u; };
 
     uint32_t ring_idx = 0;
     uint32_t p_cnt[kQTiles] = {0, 0};
@@ -327,25 +362,23 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
         // no tcgen05 fence is needed after these waits
         if (!wait_bar(FP8 ? &c.bar.q_conv[qb] : &c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
-        // S for the first kv tile
-        const uint32_t rk = ring_idx++;
-        if (!wait_full(rk))
+        // S for the first kv tile (its K and V landed together)
+        uint32_t cur = ring_idx++;
+        if (!wait_full(cur))
             break;
         if (leader) {
             for (int t = 0; t < nq; ++t) {
-                issue_s(qb, t, rk % C::kStages);
+                issue_s(qb, t, k_slot(cur));
                 mma_commit(&c.bar.s_full[t]);
             }
-            mma_commit(&empty[rk % C::kStages]);
             if (it.g.n_lo == it.g.n_hi)
                 mma_commit(&c.bar.q_empty[qb]);
         }
         __syncwarp();
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
             const bool last = j == it.g.n_hi;
-            const uint32_t rv = ring_idx++;
-            const uint32_t rk2 = last ? 0u : ring_idx++;
-            if (!wait_full(rv)) {
+            const uint32_t next = last ? 0u : ring_idx++;
+            if (FP8 && !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c.abort_flag, p.err)) {
                 ok = false;
                 break;
             }
@@ -354,7 +387,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 // loaded); zero them so that P = 0 there cannot meet a NaN.
                 const int r0 = it.kv_len - j * kKvTile;
                 if (r0 < kKvTile) {
-                    uint8_t* vt = c.base + C::kOffRing + (rv % C::kStages) * C::kKvTileBytes;
+                    uint8_t* vt = c.base + C::kOffRing + v_slot(cur) * C::kKvTileBytes;
                     const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
                     for (int h = 0; h < C::kHalves; ++h) {
                         uint4* dst = reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + r0 * 128);
@@ -373,7 +406,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     }
                     tc_fence_after();
                     if (leader)
-                        issue_pv(t, part, rv % C::kStages, j > it.g.n_lo);
+                        issue_pv(t, part, v_slot(cur), j > it.g.n_lo);
                     __syncwarp();
                 }
                 if (!ok)
@@ -381,30 +414,28 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 ++p_cnt[t];
                 if (leader) {
                     if (t == nq - 1)
-                        mma_commit(&empty[rv % C::kStages]);
+                        mma_commit(&empty[cur % C::kPairs]);  // K and V of tile j consumed
                     if (last)
                         mma_commit(&c.bar.o_full[t]);
                 }
                 __syncwarp();
                 if (!last) {
                     if (t == 0) {
-                        if (!wait_full(rk2)) {
+                        if (!wait_full(next)) {
                             ok = false;
                             break;
                         }
                     }
                     if (leader) {
-                        issue_s(qb, t, rk2 % C::kStages);
+                        issue_s(qb, t, k_slot(next));
                         mma_commit(&c.bar.s_full[t]);
-                        if (t == nq - 1) {
-                            mma_commit(&empty[rk2 % C::kStages]);
-                            if (j + 1 == it.g.n_hi)
-                                mma_commit(&c.bar.q_empty[qb]);
-                        }
+                        if (t == nq - 1 && j + 1 == it.g.n_hi)
+                            mma_commit(&c.bar.q_empty[qb]);
                     }
                     __syncwarp();
                 }
             }
+            cur = next;
         }
     }
     // every MMA this thread issued has completed once the drain barrier flips
@@ -678,15 +709,20 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
             mbar_arrive(&c.bar.q_conv[qb]);
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
             const bool zero = j * kKvTile + ct >= it.kv_len;
+            // the ring pair of this tile: K into entry 2m, V into 2m + 1
+            const uint32_t m = r % C::kPairs;
+            if (!wait_bar(&c.bar.empty[m], ((r / C::kPairs) & 1) ^ 1, c.abort_flag, p.err)) {
+                ok = false;
+                break;
+            }
             for (int kind = 0; kind < 2; ++kind) {
-                const uint32_t s8 = r8 % C::kF8Stages, s = r % C::kStages;
-                if (!wait_bar(&c.bar.f8full[s8], (r8 / C::kF8Stages) & 1, c.abort_flag, p.err) ||
-                    !wait_bar(&c.bar.empty[s], ((r / C::kStages) & 1) ^ 1, c.abort_flag, p.err)) {
+                const uint32_t s8 = r8 % C::kF8Stages;
+                if (!wait_bar(&c.bar.f8full[s8], (r8 / C::kF8Stages) & 1, c.abort_flag, p.err)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* src = c.base + C::kOffF8 + s8 * C::kF8TileBytes + ct * 128;
-                uint8_t* dst = c.base + C::kOffRing + s * C::kKvTileBytes + ct * 128;
+                uint8_t* dst = c.base + C::kOffRing + (2 * m + kind) * C::kKvTileBytes + ct * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {  // 16 e4m3 values = d 16q .. 16q+15
                     uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
@@ -709,12 +745,12 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&c.bar.full[s]);
+                    mbar_arrive(kind == 0 ? &c.bar.full[m] : &c.bar.vfull[m]);  // K lets Q K^T start early
                     mbar_arrive(&c.bar.f8empty[s8]);
                 }
                 ++r8;
-                ++r;
             }
+            ++r;  // one ring pair per tile
         }
     }
 }
@@ -731,8 +767,9 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     Ctx c;
     c.base = base;
     c.bar.full = bars;
-    c.bar.empty = c.bar.full + C::kStages;
-    c.bar.f8full = c.bar.empty + C::kStages;
+    c.bar.empty = c.bar.full + C::kPairs;
+    c.bar.vfull = c.bar.empty + C::kPairs;
+    c.bar.f8full = c.bar.vfull + (FP8 ? C::kPairs : 0);
     c.bar.f8empty = c.bar.f8full + C::kF8Stages;
     c.bar.q_full = c.bar.f8empty + C::kF8Stages;
     c.bar.q_empty = c.bar.q_full + C::kQBufs;
@@ -749,9 +786,11 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kPairs; ++s) {
             mbar_init(&c.bar.full[s], FP8 ? 4 : 1);
             mbar_init(&c.bar.empty[s], 1);
+            if (FP8)
+                mbar_init(&c.bar.vfull[s], 4);
         }
         for (int s = 0; s < C::kF8Stages; ++s) {
             mbar_init(&c.bar.f8full[s], 1);
