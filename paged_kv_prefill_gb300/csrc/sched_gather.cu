@@ -60,10 +60,11 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     pdl_launch_dependents();
     extern __shared__ int sm[];
     const int B = p.B;
-    int* hist = sm;                                  // [32 warps][kSchedBuckets]
-    int* scratch = hist + 32 * kSchedBuckets;        // 64
-    int* tot = scratch + 64;                         // [kSchedBuckets]
-    int* req_start = tot + kSchedBuckets;            // [B + 1] first item of each request
+    const int nb = p.nbuckets;
+    int* hist = sm;                                  // [32 warps][nb]
+    int* scratch = hist + 32 * nb;                   // 64
+    int* tot = scratch + 64;                         // [nb]
+    int* req_start = tot + nb;                       // [B + 1] first item of each request
     int* req_q = req_start + B + 1;                  // [B] q_len
     int* req_kv = req_q + B;                         // [B] kv_len
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -98,9 +99,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             }
         }
     }
-    const int nb = p.nbuckets;
     for (int k = tid; k < 32 * nb; k += kSchedThreads)
-        hist[(k / nb) * kSchedBuckets + k % nb] = 0;
+        hist[k] = 0;
     int n_total = 0;
     int run = block_exclusive_scan(local, scratch, &n_total);
     for (int b = b_begin; b < b_end; ++b) {
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
 
     const int seg = (n_total + 31) / 32;
     const int s_begin = min(n_total, warp * seg), s_end = min(n_total, s_begin + seg);
-    int* my_hist = hist + warp * kSchedBuckets;
+    int* my_hist = hist + warp * nb;
 
     // 2. per-warp bucket counts
     for (int base = s_begin; base < s_end; base += 32) {
@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         const int c = tid;  // nb <= kSchedBuckets == kSchedThreads
         int acc = 0;
         for (int w = 0; w < 32; ++w) {
-            const int v = hist[w * kSchedBuckets + c];
-            hist[w * kSchedBuckets + c] = acc;
+            const int v = hist[w * nb + c];
+            hist[w * nb + c] = acc;
             acc += v;
         }
         tot[c] = acc;
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     if (tid < nb) {
         const int c = nb - 1 - tid;
         for (int w = 0; w < 32; ++w)
-            hist[w * kSchedBuckets + c] += start;
+            hist[w * nb + c] += start;
     }
     __syncthreads();
 
@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
 {
-    const size_t smem = sizeof(int) * ((size_t)32 * kSchedBuckets + 64 + kSchedBuckets + 3 * (size_t)p.B + 1);
+    const size_t nb = (size_t)p.nbuckets;
+    const size_t smem = sizeof(int) * (32 * nb + 64 + nb + 3 * (size_t)p.B + 1);
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
