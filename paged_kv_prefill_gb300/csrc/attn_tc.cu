@@ -291,7 +291,8 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer: warp 1, lane 0 issues; the whole warp waits.
+// MMA issuer: warp 1.  The whole warp waits and runs the issue code; the
+// MMAs and commits are predicated on lane 0, so the warp never diverges.
 // ---------------------------------------------------------------------------
 template <int D, bool FP8>
 __device__ void mma_role(const AttnParams& p, const Ctx& c)
@@ -305,6 +306,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                                  ((uint32_t)(kQRows >> 4) << 24);
     const int lane = threadIdx.x & 31;
     const bool leader = lane == 0;
+    const uint32_t issue = leader ? 1u : 0u;  // lane 0 issues; the warp stays converged
     const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
     const uint32_t ring = smem_u32(c.base + C::kOffRing);
     uint64_t* const full = c.bar.full;
@@ -326,7 +328,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (uint32_t)((k / 4) * kHalfW + (k % 4) * 2);  // 16 elements = 32 B
-            mma_ss_w(d, a0 + off, b0 + off, kHi, kIdescS, k > 0 ? 1u : 0u);
+            mma_ss_wp(d, a0 + off, b0 + off, kHi, kIdescS, k > 0 ? 1u : 0u, issue);
         }
     };
     // P V over the keys of part `part` of the tile
@@ -338,7 +340,8 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
 #pragma unroll
         for (int kk = 0; kk < kSteps; ++kk) {
             const int k = part * kSteps + kk;                          // 16 keys = 16 rows of 128 B
-            mma_ts_w(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u);
+            mma_ts_wp(d, a + (uint32_t)(k * 8), b0 + (uint32_t)(k * 128), kHi, kIdescO, (acc || k > 0) ? 1u : 0u,
+                      issue);
         }
     };
     // ring pair r % kPairs holds K (entry 2m) and V (entry 2m + 1) of the r-th tile
@@ -366,15 +369,12 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
         uint32_t cur = ring_idx++;
         if (!wait_full(cur))
             break;
-        if (leader) {
-            for (int t = 0; t < nq; ++t) {
-                issue_s(qb, t, k_slot(cur));
-                mma_commit(&c.bar.s_full[t]);
-            }
-            if (it.g.n_lo == it.g.n_hi)
-                mma_commit(&c.bar.q_empty[qb]);
+        for (int t = 0; t < nq; ++t) {
+            issue_s(qb, t, k_slot(cur));
+            mma_commit_p(&c.bar.s_full[t], issue);
         }
-        __syncwarp();
+        if (it.g.n_lo == it.g.n_hi)
+            mma_commit_p(&c.bar.q_empty[qb], issue);
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
             const bool last = j == it.g.n_hi;
             const uint32_t next = last ? 0u : ring_idx++;
@@ -405,20 +405,15 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                         break;
                     }
                     tc_fence_after();
-                    if (leader)
-                        issue_pv(t, part, v_slot(cur), j > it.g.n_lo);
-                    __syncwarp();
+                    issue_pv(t, part, v_slot(cur), j > it.g.n_lo);
                 }
                 if (!ok)
                     break;
                 ++p_cnt[t];
-                if (leader) {
-                    if (t == nq - 1)
-                        mma_commit(&empty[cur % C::kPairs]);  // K and V of tile j consumed
-                    if (last)
-                        mma_commit(&c.bar.o_full[t]);
-                }
-                __syncwarp();
+                if (t == nq - 1)
+                    mma_commit_p(&empty[cur % C::kPairs], issue);  // K and V of tile j consumed
+                if (last)
+                    mma_commit_p(&c.bar.o_full[t], issue);
                 if (!last) {
                     if (t == 0) {
                         if (!wait_full(next)) {
@@ -426,13 +421,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                             break;
                         }
                     }
-                    if (leader) {
-                        issue_s(qb, t, k_slot(next));
-                        mma_commit(&c.bar.s_full[t]);
-                        if (t == nq - 1 && j + 1 == it.g.n_hi)
-                            mma_commit(&c.bar.q_empty[qb]);
-                    }
-                    __syncwarp();
+                    issue_s(qb, t, k_slot(next));
+                    mma_commit_p(&c.bar.s_full[t], issue);
+                    if (t == nq - 1 && j + 1 == it.g.n_hi)
+                        mma_commit_p(&c.bar.q_empty[qb], issue);
                 }
             }
             cur = next;
