@@ -534,12 +534,10 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             // keep a stale maximum until the row maximum grows by more than 2^8:
             // exact, since the denominator uses the same stale maximum
             const bool need = m_tile > m_used + 8.0f;
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2_approx(m_used - m_tile);
-                l *= alpha;
-                m_used = m_tile;
-            }
+            // branch-free, so the warp does not diverge on rows whose maximum grew
+            const float alpha = need ? ex2_approx(m_used - m_tile) : 1.f;
+            l *= alpha;
+            m_used = need ? m_tile : m_used;
             const float neg = m_used == -INFINITY ? 0.f : -m_used;
             const float2 sc = make_float2(sl2, sl2), ng = make_float2(neg, neg);
             float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -601,8 +599,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&c.bar.p_full[C::kPParts * t + part]);
+                mbar_arrive_p(&c.bar.p_full[C::kPParts * t + part], lane == 0 ? 1u : 0u);
             }
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a = __fadd2_rn(a01, a23);

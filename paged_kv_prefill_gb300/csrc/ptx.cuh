@@ -34,6 +34,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
                  : "memory");
 }
 
+// mbar_arrive executed by a whole warp, arriving only from lanes with issue != 0.
+__device__ __forceinline__ void mbar_arrive_p(uint64_t* bar, uint32_t issue)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+                 "@q mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar)),
+                 "r"(issue)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
 {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
