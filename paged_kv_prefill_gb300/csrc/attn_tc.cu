@@ -243,19 +243,16 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
                     ok = false;
                     break;
                 }
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&c.bar.full[m], 2 * bytes);
+                // predicated rather than branched: the warp stays converged
+                mbar_arrive_expect_tx_p(&c.bar.full[m], 2 * bytes, lane == 0 ? 1u : 0u);
                 __syncwarp();
-                if (valid) {
 #pragma unroll
-                    for (int kind = 0; kind < 2; ++kind) {
-                        const uint32_t dst =
-                            ring + (2 * m + kind) * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
+                for (int kind = 0; kind < 2; ++kind) {
+                    const uint32_t dst = ring + (2 * m + kind) * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
 #pragma unroll
-                        for (int h = 0; h < kBoxes; ++h)
-                            tma_load_4d(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &c.bar.full[m], h * 64,
-                                        slot0, it.kvh, page);
-                    }
+                    for (int h = 0; h < kBoxes; ++h)
+                        tma_load_4d_p(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &c.bar.full[m], h * 64, slot0,
+                                      it.kvh, page, valid ? 1u : 0u);
                 }
                 ++ring_idx;
             } else {

@@ -99,6 +99,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// tma_load_4d executed by a whole warp, issuing only from lanes with issue != 0.
+__device__ __forceinline__ void tma_load_4d_p(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
+                                              int c2, int c3, uint32_t issue)
+{
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %7, 0;\n\t"
+        "@q cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(issue)
+        : "memory");
+}
+
+// mbar_arrive_expect_tx executed by a whole warp, arriving only from lanes with issue != 0.
+__device__ __forceinline__ void mbar_arrive_expect_tx_p(uint64_t* bar, uint32_t bytes, uint32_t issue)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+                 "@q mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+                 "r"(bytes), "r"(issue)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- PDL (PTX ISA: griddepcontrol)
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
