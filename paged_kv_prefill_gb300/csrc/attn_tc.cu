@@ -351,29 +351,56 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     uint32_t ring_idx = 0;
     uint32_t p_cnt[kQTiles] = {0, 0};
     bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
-        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
-        if (w < 0)
-            break;
+
+    // An open item: its Q landed and its first kv tile (ring entry `first`) too.
+    struct Open {
+        int n_lo, n_hi, nq, kv_len;
+        uint32_t qb, first;
+        bool ok;
+    };
+    auto open_item = [&](int w, uint32_t n) -> Open {
         const ItemInfo it = read_item(p, w);
-        const int nq = it.g.nq;
-        const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
+        Open o;
+        o.n_lo = it.g.n_lo;
+        o.n_hi = it.g.n_hi;
+        o.nq = it.g.nq;
+        o.kv_len = it.kv_len;
+        o.qb = n % C::kQBufs;
         // TMA (and converter) writes reach the MMA through the mbarrier alone:
         // no tcgen05 fence is needed after these waits
-        if (!wait_bar(FP8 ? &c.bar.q_conv[qb] : &c.bar.q_full[qb], qph, c.abort_flag, p.err))
-            break;
-        // S for the first kv tile (its K and V landed together)
-        uint32_t cur = ring_idx++;
-        if (!wait_full(cur))
-            break;
-        for (int t = 0; t < nq; ++t) {
-            issue_s(qb, t, k_slot(cur));
-            mma_commit_p(&c.bar.s_full[t], issue);
-        }
-        if (it.g.n_lo == it.g.n_hi)
-            mma_commit_p(&c.bar.q_empty[qb], issue);
-        for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
-            const bool last = j == it.g.n_hi;
+        o.ok = wait_bar(FP8 ? &c.bar.q_conv[o.qb] : &c.bar.q_full[o.qb], (n / C::kQBufs) & 1, c.abort_flag, p.err);
+        o.first = ring_idx++;
+        o.ok = o.ok && wait_full(o.first);
+        return o;
+    };
+    // S_t of an open item's first kv tile
+    auto first_s = [&](const Open o, int t) {
+        issue_s(o.qb, t, k_slot(o.first));
+        mma_commit_p(&c.bar.s_full[t], issue);
+        if (t == o.nq - 1 && o.n_lo == o.n_hi)
+            mma_commit_p(&c.bar.q_empty[o.qb], issue);
+    };
+
+    // The next item is opened while the current one's last kv tile finishes:
+    // its S_0 right after the last P_0 V, its S_1 after the last P_1 V, the
+    // same order as between two kv tiles of one item.
+    Open cur_item;
+    int w = take_item<C::kItemSlots>(p, c, 0, &ok);
+    if (w >= 0) {
+        cur_item = open_item(w, 0);
+        ok = cur_item.ok;
+        for (int t = 0; ok && t < cur_item.nq; ++t)
+            first_s(cur_item, t);
+    }
+    for (uint32_t n = 0; ok && w >= 0; ++n) {
+        const int n_lo = cur_item.n_lo, n_hi = cur_item.n_hi, kv_len = cur_item.kv_len;
+        const int nq = cur_item.nq;
+        const uint32_t qb = cur_item.qb;
+        uint32_t cur = cur_item.first;
+        Open nxt;
+        int w_next = -1;
+        for (int j = n_lo; ok && j <= n_hi; ++j) {
+            const bool last = j == n_hi;
             const uint32_t next = last ? 0u : ring_idx++;
             if (FP8 && !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c.abort_flag, p.err)) {
                 ok = false;
@@ -382,7 +409,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
             if (!FP8) {
                 // keys >= kv_len: V rows may hold any bits (or a page that was not
                 // loaded); zero them so that P = 0 there cannot meet a NaN.
-                const int r0 = it.kv_len - j * kKvTile;
+                const int r0 = kv_len - j * kKvTile;
                 if (r0 < kKvTile) {
                     uint8_t* vt = c.base + C::kOffRing + v_slot(cur) * C::kKvTileBytes;
                     const int n16 = (kKvTile - r0) * 8;  // 16-byte chunks per column block
@@ -402,7 +429,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                         break;
                     }
                     tc_fence_after();
-                    issue_pv(t, part, v_slot(cur), j > it.g.n_lo);
+                    issue_pv(t, part, v_slot(cur), j > n_lo);
                 }
                 if (!ok)
                     break;
@@ -420,12 +447,32 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     }
                     issue_s(qb, t, k_slot(next));
                     mma_commit_p(&c.bar.s_full[t], issue);
-                    if (t == nq - 1 && j + 1 == it.g.n_hi)
+                    if (t == nq - 1 && j + 1 == n_hi)
                         mma_commit_p(&c.bar.q_empty[qb], issue);
+                } else if (t == 0) {
+                    w_next = take_item<C::kItemSlots>(p, c, n + 1, &ok);
+                    if (!ok)
+                        break;
+                    if (w_next >= 0) {
+                        nxt = open_item(w_next, n + 1);
+                        if (!nxt.ok) {
+                            ok = false;
+                            break;
+                        }
+                        first_s(nxt, 0);
+                        if (nq == 1 && nxt.nq > 1)
+                            first_s(nxt, 1);  // no P_1 V to wait for in this item
+                    }
+                } else if (w_next >= 0 && nxt.nq > 1) {
+                    first_s(nxt, 1);
                 }
             }
             cur = next;
         }
+        if (!ok)
+            break;
+        w = w_next;
+        cur_item = nxt;
     }
     // every MMA this thread issued has completed once the drain barrier flips
     if (leader)
@@ -835,30 +882,30 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
 
     if constexpr (FP8) {
         // 512 threads launch with 128 registers each; the softmax warpgroups
-        // take registers from the others (64 + 184 + 184 + 80 = 512 = 4 x 128)
+        // take registers from the others (96 + 176 + 176 + 64 = 512 = 4 x 128)
         if (warp < 4) {
-            regs_dec<64>();
+            regs_dec<96>();
             if (warp == 0)
                 producer_role<D, FP8>(p, c);
             else if (warp == 1)
                 mma_role<D, FP8>(p, c);
         } else if (warp < 12) {
-            regs_inc<184>();
+            regs_inc<176>();
             softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
         } else {
-            regs_dec<80>();
+            regs_dec<64>();
             convert_role<D, FP8>(p, c);
         }
     } else {
-        // 384 threads launch with 168 registers each (64 + 216 + 216 = 496 <= 3 x 168)
+        // 384 threads launch with 168 registers each (96 + 200 + 200 = 496 <= 3 x 168)
         if (warp < 4) {
-            regs_dec<64>();
+            regs_dec<96>();
             if (warp == 0)
                 producer_role<D, FP8>(p, c);
             else if (warp == 1)
                 mma_role<D, FP8>(p, c);
         } else {
-            regs_inc<216>();
+            regs_inc<200>();
             softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
         }
     }
