@@ -449,7 +449,9 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     mma_commit_p(&c.bar.s_full[t], issue);
                     if (t == nq - 1 && j + 1 == n_hi)
                         mma_commit_p(&c.bar.q_empty[qb], issue);
-                } else if (t == 0) {
+                } else if (t == (FP8 ? nq - 1 : 0)) {
+                    // (FP8: after the last P V, since the next item's Q and K wait
+                    // for the converter warps)
                     w_next = take_item<C::kItemSlots>(p, c, n + 1, &ok);
                     if (!ok)
                         break;
@@ -460,10 +462,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                             break;
                         }
                         first_s(nxt, 0);
-                        if (nq == 1 && nxt.nq > 1)
-                            first_s(nxt, 1);  // no P_1 V to wait for in this item
+                        if ((FP8 || nq == 1) && nxt.nq > 1)
+                            first_s(nxt, 1);  // no P_1 V left to wait for in this item
                     }
-                } else if (w_next >= 0 && nxt.nq > 1) {
+                } else if (!FP8 && w_next >= 0 && nxt.nq > 1) {
                     first_s(nxt, 1);
                 }
             }
