@@ -33,7 +33,7 @@
  *    backends/trtllm.py, _init_extend_metadata; TensorRT-LLM teardown (6),
  *    section "步骤三" kv_lens = cached + new).
  *
- * Readings where the pages leave a point open (each is listed in the design doc):
+ * Readings taken where the pages leave a point open:
  *  - a query head h uses kv head h / (num_heads / num_kv_heads);
  *  - window_left = W >= 0 keeps keys j with pos - W <= j <= pos (W + 1 keys);
  *  - sinks are in the units of the scaled logits (after bmm1_scale) and add
