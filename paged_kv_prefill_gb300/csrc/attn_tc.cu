@@ -422,7 +422,11 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     __syncwarp();
                 }
             }
-            for (int t = 0; ok && t < nq; ++t) {
+            // unrolled over the two query tiles, so p_cnt[t] stays in registers
+#pragma unroll
+            for (int t = 0; t < kQTiles; ++t) {
+                if (!ok || t >= nq)
+                    break;
                 for (int part = 0; part < C::kPParts; ++part) {
                     if (!wait_bar(&c.bar.p_full[C::kPParts * t + part], p_cnt[t] & 1, c.abort_flag, p.err)) {
                         ok = false;
