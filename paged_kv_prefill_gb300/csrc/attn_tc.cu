@@ -563,23 +563,37 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             if (interior) {
                 mx = fmax3(fmax3(mq[0], mq[1], mq[2]), mq[3], -INFINITY);
             } else {
+                // per 32-key chunk, decided for the whole warp: every row sees all of
+                // it (its ld.red maximum stands), no row sees any of it (maximum
+                // -inf; the exponential loop below skips it on the same test, so
+                // its scores are never read), or mask element by element
+                float cm[4];
 #pragma unroll
-                for (int k = 0; k < kKvTile; ++k) {
-                    const int key = k0 + k;
-                    if (key < lo || key > hi)
-                        s[k] = -INFINITY;
+                for (int q = 0; q < 4; ++q) {
+                    const int c0 = k0 + 32 * q;
+                    if (__all_sync(0xffffffffu, c0 >= lo && c0 + 31 <= hi)) {
+                        cm[q] = mq[q];
+                    } else if (__all_sync(0xffffffffu, c0 > hi || c0 + 31 < lo)) {
+                        cm[q] = -INFINITY;
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int key = c0 + k;
+                            if (key < lo || key > hi)
+                                s[32 * q + k] = -INFINITY;
+                        }
+                        // two independent 3-input max chains over the chunk
+                        float m0 = fmax3(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+                        float m1 = fmax3(s[32 * q + 16], s[32 * q + 17], s[32 * q + 18]);
+#pragma unroll
+                        for (int k = 3; k < 15; k += 2) {
+                            m0 = fmax3(m0, s[32 * q + k], s[32 * q + k + 1]);
+                            m1 = fmax3(m1, s[32 * q + 16 + k], s[32 * q + 16 + k + 1]);
+                        }
+                        cm[q] = fmax3(m0, m1, fmaxf(s[32 * q + 15], s[32 * q + 31]));
+                    }
                 }
-                // masked row maximum: eight independent 3-input max chains
-                float pm[8];
-#pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    float m = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
-#pragma unroll
-                    for (int k = 3; k < 15; k += 2)
-                        m = fmax3(m, s[16 * a + k], s[16 * a + k + 1]);
-                    pm[a] = fmaxf(m, s[16 * a + 15]);
-                }
-                mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+                mx = fmax3(fmax3(cm[0], cm[1], cm[2]), cm[3], -INFINITY);
             }
             const float m_tile = mx * sl2;
             // keep a stale maximum until the row maximum grows by more than 2^8:
