@@ -16,7 +16,8 @@ namespace b2pa {
 //    the largest possible cost needs, so bucket = cost unless the cost reaches
 //    kCostCap): each warp owns a contiguous
 //    slice of the enumeration, counts per bucket with __match_any_sync,
-//    bucket starts come from a scan over (bucket descending, warp ascending),
+//    a warp-shuffle scan over the warps gives each warp's offset within a
+//    bucket, a block scan over the buckets (descending) gives their starts,
 //    and a second pass scatters each item to its rank.  The order is fully
 //    deterministic.
 // Writes items[0 .. n) and *count = n; sets B2PA_DEV_BAD_REQUEST for
@@ -155,25 +156,28 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     }
     __syncthreads();
 
-    // 3. offsets: buckets in descending order, warps in ascending order
-    if (tid < nb) {
-        const int c = tid;  // nb <= kSchedBuckets == kSchedThreads
-        int acc = 0;
-        for (int w = 0; w < 32; ++w) {
-            const int v = hist[w * nb + c];
-            hist[w * nb + c] = acc;
-            acc += v;
+    // 3. offsets: buckets in descending order, warps in ascending order.
+    // Within a bucket, the warps' counts are scanned by one warp (lane w holds
+    // warp w's count); warp u takes buckets u, u + 32, ...
+    for (int c = warp; c < nb; c += 32) {
+        const int v = hist[lane * nb + c];
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
         }
-        tot[c] = acc;
+        hist[lane * nb + c] = x - v;
+        if (lane == 31)
+            tot[c] = x;
     }
     __syncthreads();
     // exclusive scan over buckets from the top: thread t takes bucket nb - 1 - t
+    // (nb <= kSchedBuckets == kSchedThreads); tot then holds each bucket's start
     const int start = block_exclusive_scan(tid < nb ? tot[nb - 1 - tid] : 0, scratch, nullptr);
-    if (tid < nb) {
-        const int c = nb - 1 - tid;
-        for (int w = 0; w < 32; ++w)
-            hist[w * nb + c] += start;
-    }
+    if (tid < nb)
+        tot[nb - 1 - tid] = start;
     __syncthreads();
 
     // 4. scatter
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         const unsigned grp = __match_any_sync(0xffffffffu, bucket);
         const unsigned lower = grp & ((1u << lane) - 1u);
         if (bucket >= 0) {
-            const int pos = my_hist[bucket] + __popc(lower);
+            const int pos = tot[bucket] + my_hist[bucket] + __popc(lower);
             if (pos < p.cap)
                 p.items[pos] = item;
         }
