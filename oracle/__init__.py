@@ -63,6 +63,9 @@ def _load():
         lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.oracle_bf16_value.restype = ctypes.c_double
         lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_append_kv.restype = ctypes.c_int64
         _lib = lib
     return _lib
 
@@ -94,6 +97,30 @@ def e4m3_value(code: int) -> float:
 
 def bf16_value(bits: int) -> float:
     return _load().oracle_bf16_value(bits)
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code to the binary32 value x (ties to the even code, +-448 saturation)."""
+    return _load().oracle_e4m3_encode(x)
+
+
+def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+              cache_loc: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0, layout: str = "HND") -> int:
+    """Write token n's K/V rows ([T, Hkv, D] bf16) into slot cache_loc[n] of the CPU pools, in place.
+
+    Returns the number of tokens whose slot lies outside the pool (not written).
+    """
+    lib = _load()
+    assert k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16 and k_new.dim() == 3
+    assert k_new.shape == v_new.shape and k_new.stride() == v_new.stride() and k_new.stride(2) == 1
+    loc = cache_loc.to(torch.int32).contiguous()
+    assert loc.numel() == k_new.shape[0]
+    kp, vp = _pool(k_pool), _pool(v_pool)
+    return int(lib.oracle_append_kv(
+        _ptr(k_new), _ptr(v_new), ctypes.c_int64(k_new.shape[0]), ctypes.c_int64(k_new.stride(0)),
+        ctypes.c_int64(k_new.stride(1)), _ptr(loc), ctypes.byref(kp), ctypes.byref(vp),
+        ctypes.c_int(LAYOUTS[layout]), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+    ))
 
 
 def attention(inp, rows=None, threads: int | None = None):

@@ -389,3 +389,86 @@ int oracle_worklist(const int32_t* cum_q, const int32_t* seq_lens, int B, int nu
     free(tmp);
     return (int)n;
 }
+
+/*
+ * Writing new tokens' K and V into the paged pools: the step before the
+ * attention in the TokenSpeed trtllm backend (_save_kv_and_prepare_q), which
+ * calls fused_fp8_set_kv_buffer(k, v, k_cache, v_cache, cache_loc, k_scale,
+ * v_scale, page_size) for an e4m3 cache and set_kv_buffer otherwise.  Token n's
+ * rows k[n, h, :] and v[n, h, :] go to cache slot cache_loc[n]: page
+ * cache_loc[n] / page_size, slot cache_loc[n] % page_size (the page / slot
+ * addressing of the attention's gather above).
+ *
+ * Readings (the pages print the call, not its kernel):
+ *  - a bf16 pool receives the bf16 values unchanged; the scales apply to an
+ *    e4m3 pool only;
+ *  - an e4m3 pool receives x / scale, the quotient taken in IEEE binary32,
+ *    rounded to the nearest e4m3 value with ties to the even code; magnitudes
+ *    above the largest finite value, 448, saturate to it;
+ *  - a slot outside [0, num_pages * page_size) is not written.
+ */
+
+/* Nearest e4m3 code to x.  The non-negative finite codes 0x00 .. 0x7E have
+ * increasing values, so a binary search finds the largest code whose value is
+ * not above |x|; the answer is the nearer of it and the next code, the even
+ * one on a tie.  NaN maps to 0x7F. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (oracle_e4m3_value((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double below = a - oracle_e4m3_value((uint8_t)lo), above = oracle_e4m3_value((uint8_t)hi) - a;
+    int c = below < above ? lo : (above < below ? hi : ((lo & 1) ? hi : lo));
+    return sign | (uint8_t)c;
+}
+
+static void store_elem(const oracle_pool* p, int64_t off, uint16_t bits, float scale)
+{
+    if (p->dtype == OR_BF16) {
+        ((uint16_t*)p->data)[off] = bits;
+    } else {
+        float x = (float)bf16_value(bits); /* exact */
+        float q = x / scale;               /* one binary32 division */
+        ((uint8_t*)p->data)[off] = oracle_e4m3_encode(q);
+    }
+}
+
+/* k_new / v_new: bf16 [T, num_kv_heads, head_dim], element strides st_tok,
+ * st_head, head_dim contiguous.  The pools are written in place.  Returns the
+ * number of tokens whose slot lies outside the pool. */
+int64_t oracle_append_kv(const uint16_t* k_new, const uint16_t* v_new, int64_t T, int64_t st_tok,
+                         int64_t st_head, const int32_t* cache_loc, const oracle_pool* k_pool,
+                         const oracle_pool* v_pool, int layout, float k_scale, float v_scale)
+{
+    int P = pool_page_size(k_pool, layout);
+    int H = pool_kv_heads(k_pool, layout);
+    int D = (int)k_pool->shape[3];
+    int64_t slots = k_pool->shape[0] * (int64_t)P;
+    int64_t outside = 0;
+    for (int64_t n = 0; n < T; ++n) {
+        int64_t loc = cache_loc[n];
+        if (loc < 0 || loc >= slots) {
+            ++outside;
+            continue;
+        }
+        int64_t page = loc / P, slot = loc % P;
+        for (int h = 0; h < H; ++h)
+            for (int d = 0; d < D; ++d) {
+                int64_t src = n * st_tok + (int64_t)h * st_head + d;
+                store_elem(k_pool, pool_offset(k_pool, layout, page, h, slot, d), k_new[src], k_scale);
+                store_elem(v_pool, pool_offset(v_pool, layout, page, h, slot, d), v_new[src], v_scale);
+            }
+    }
+    return outside;
+}

@@ -365,6 +365,134 @@ def test_worklist_skips_invalid_requests():
     assert set(got[:, 0].tolist()) == {0}
 
 
+# ---------------------------------------------------------------- the K/V write before the attention
+
+def _e4m3_codes_torch(x: torch.Tensor) -> torch.Tensor:
+    """torch's binary32 -> e4m3 cast (round to nearest even), as raw codes."""
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def test_e4m3_encoder_round_trips_every_finite_code():
+    for c in range(256):
+        if c & 0x7F == 0x7F:  # the two NaN codes
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, hex(c)
+
+
+def test_e4m3_encoder_breaks_ties_to_the_even_code():
+    for c in range(0x7E):
+        lo, hi = oracle.e4m3_value(c), oracle.e4m3_value(c + 1)
+        mid = np.float32((lo + hi) / 2)  # exact: e4m3 values carry at most 4 significant bits
+        assert float(mid) == (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(float(mid)) == even, hex(c)
+        assert oracle.e4m3_encode(-float(mid)) == 0x80 | even, hex(c)
+        below = np.nextafter(mid, np.float32(-1.0))
+        above = np.nextafter(mid, np.float32(1e9))
+        assert oracle.e4m3_encode(float(below)) == c and oracle.e4m3_encode(float(above)) == c + 1, hex(c)
+
+
+def test_e4m3_encoder_matches_torch_cast_in_range():
+    g = torch.Generator().manual_seed(77)
+    uniform = (torch.rand(20000, generator=g, dtype=torch.float64) * 2 - 1) * 448
+    sign = torch.where(torch.rand(20000, generator=g) < 0.5, -1.0, 1.0).double()
+    spread = torch.exp(torch.rand(20000, generator=g, dtype=torch.float64) * 25 - 19).clamp(max=448) * sign
+    x = torch.cat([uniform, spread]).float()
+    got = torch.tensor([oracle.e4m3_encode(v) for v in x.tolist()], dtype=torch.uint8)
+    assert torch.equal(got, _e4m3_codes_torch(x))
+
+
+def test_e4m3_encoder_saturates_at_448():
+    for v in [448.0, 449.0, 463.0, 464.0, 465.0, 1.0e4, 3.0e38]:
+        assert oracle.e4m3_encode(v) == 0x7E and oracle.e4m3_encode(-v) == 0xFE, v
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def _append_case(layout, fp8, T=40, N=12, P=8, H=3, D=16, seed=5):
+    g = torch.Generator().manual_seed(seed)
+    shape = (N, H, P, D) if layout == "HND" else (N, P, H, D)
+    if fp8:
+        kp = torch.randint(0, 0x7E, shape, generator=g, dtype=torch.uint8).view(torch.float8_e4m3fn)
+        vp = torch.randint(0x80, 0xFE, shape, generator=g, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    else:
+        kp = torch.randn(shape, generator=g).to(torch.bfloat16)
+        vp = torch.randn(shape, generator=g).to(torch.bfloat16)
+    k_new = (torch.randn((T, H, D), generator=g) * 3).to(torch.bfloat16)
+    v_new = (torch.randn((T, H, D), generator=g) * 2).to(torch.bfloat16)
+    loc = torch.randperm(N * P, generator=g)[:T].to(torch.int32)
+    return kp, vp, k_new, v_new, loc
+
+
+def _written_by_indexing(pool, new, loc, layout, scale):
+    """The pool after the write, by torch indexing (and torch's cast, after clamping to +-448)."""
+    P = pool.shape[2] if layout == "HND" else pool.shape[1]
+    fp8 = pool.dtype == torch.float8_e4m3fn
+    out = pool.clone()
+    view = out.view(torch.uint8) if fp8 else out
+    for n, s in enumerate(loc.tolist()):
+        if s < 0 or s >= pool.shape[0] * P:
+            continue
+        page, slot = s // P, s % P
+        rows = new[n]
+        if fp8:
+            rows = _e4m3_codes_torch((rows.float() / torch.tensor(scale, dtype=torch.float32)).clamp(-448, 448))
+        if layout == "HND":
+            view[page, :, slot, :] = rows
+        else:
+            view[page, slot, :, :] = rows
+    return out
+
+
+def _same_bits(a, b):
+    return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("fp8,scales", [(False, (1.0, 1.0)), (True, (0.02, 0.03)), (True, (0.013, 0.004))])
+def test_append_matches_torch_indexing(layout, fp8, scales):
+    # (0.013, 0.004): quotients up to ~900, so the saturation is exercised
+    kp, vp, k_new, v_new, loc = _append_case(layout, fp8)
+    want_k = _written_by_indexing(kp, k_new, loc, layout, scales[0])
+    want_v = _written_by_indexing(vp, v_new, loc, layout, scales[1])
+    assert oracle.append_kv(k_new, v_new, kp, vp, loc, scales[0], scales[1], layout) == 0
+    assert _same_bits(kp, want_k) and _same_bits(vp, want_v)
+
+
+def test_append_skips_slots_outside_the_pool():
+    kp, vp, k_new, v_new, loc = _append_case("HND", False, T=10)
+    loc[3] = -1
+    loc[7] = kp.shape[0] * kp.shape[2]
+    want_k = _written_by_indexing(kp, k_new, loc, "HND", 1.0)
+    assert oracle.append_kv(k_new, v_new, kp, vp, loc, 1.0, 1.0, "HND") == 2
+    assert _same_bits(kp, want_k)
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_append_then_gather_returns_the_new_tokens(layout):
+    # the new tokens of each request are its last q_len keys: positions prefix .. kv_len - 1
+    inp = workload.build([5, 17, 1], [9, 40, 33], 4, 2, 16, 8, layout, seed=31)
+    g = torch.Generator().manual_seed(32)
+    T, H, D, P = inp.q.shape[0], inp.num_kv_heads, inp.head_dim, inp.page_size
+    k_new = torch.randn((T, H, D), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((T, H, D), generator=g).to(torch.bfloat16)
+    loc = []
+    for b in range(inp.batch):
+        q_len = int(inp.cum_q[b + 1] - inp.cum_q[b])
+        kv = int(inp.seq_lens[b])
+        for t in range(kv - q_len, kv):
+            page, slot = _kv_index(inp, b, t)
+            loc.append(page * P + slot)
+    assert oracle.append_kv(k_new, v_new, inp.k_pool, inp.v_pool, torch.tensor(loc, dtype=torch.int32),
+                            1.0, 1.0, layout) == 0
+    for which, new in (("k", k_new), ("v", v_new)):
+        rows, ok = oracle.gather(inp, which)
+        assert ok
+        for b in range(inp.batch):
+            q0, q1 = int(inp.cum_q[b]), int(inp.cum_q[b + 1])
+            kv0, kv = int(inp.cum_kv[b]), int(inp.seq_lens[b])
+            assert torch.equal(rows[kv0 + kv - (q1 - q0):kv0 + kv], new[q0:q1])
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 _MUTANTS = {
@@ -384,6 +512,14 @@ _MUTANTS = {
     "bmm2": ("o[d] = bmm2_scale * acc[d] / den;", "o[d] = acc[d] / den;"),
     # e4m3 bias
     "e4m3_bias": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    # e4m3 encoding: ties to the odd code
+    "e4m3_ties_odd": ("((lo & 1) ? hi : lo)", "((lo & 1) ? lo : hi)"),
+    # e4m3 encoding: NaN instead of saturation above 448
+    "e4m3_overflow_nan": ("        return sign | 0x7E;", "        return sign | 0x7F;"),
+    # the write: scale not applied
+    "append_unscaled": ("float q = x / scale;", "float q = x;"),
+    # the write: slot within the page mirrored
+    "append_slot": ("int64_t page = loc / P, slot = loc % P;", "int64_t page = loc / P, slot = (P - 1) - loc % P;"),
 }
 
 
@@ -413,6 +549,9 @@ def _pins_pass(lib_path):
         lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.oracle_bf16_value.restype = ctypes.c_double
         lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_append_kv.restype = ctypes.c_int64
         oracle._lib = lib
         checks = [
             lambda: test_matches_torch_sdpa_fp64("HND", 3, True),
@@ -420,6 +559,10 @@ def _pins_pass(lib_path):
             lambda: test_matches_torch_sdpa_fp8_kv(),
             lambda: test_matches_torch_sdpa_gqa8_d64(),
             lambda: test_e4m3_decoder_matches_torch_all_codes(),
+            lambda: test_e4m3_encoder_breaks_ties_to_the_even_code(),
+            lambda: test_e4m3_encoder_saturates_at_448(),
+            lambda: test_append_matches_torch_indexing("NHD", True, (0.013, 0.004)),
+            lambda: test_append_then_gather_returns_the_new_tokens("HND"),
         ]
         for c in checks:
             try:
