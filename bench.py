@@ -302,6 +302,64 @@ def run_all_workloads(reps: int = 20):
                           "gflop": fl / 1e9, "algorithmic_mb": by / 1e6, "kernel_ms": k_ms, "call_ms": c_ms,
                           "kernel_tflops": fl / k_ms / 1e9, "call_tflops": fl / c_ms / 1e9,
                           "kernel_gbs": by / k_ms / 1e6, "device_status": b2pa.device_status()}), flush=True)
+    run_append_workloads(reps)
+
+
+def run_append_workloads(reps: int = 20):
+    """One JSON line per timed K/V write (the step before the attention): every new
+    token of the bench workload (bf16 pool) and of the ragged FP8 workload (e4m3
+    pool) into its slot; median device time after a 512 MiB L2 flush."""
+    import paged_kv_prefill_gb300 as b2pa
+    from paged_kv_prefill_gb300 import build as b2pa_build
+
+    b2pa_build.build()
+    b2pa.load()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    _, hbm_gbs, _ = peaks()
+    for idx in (2, 5):
+        inp = workload.config(idx)
+        T, H, D = inp.q.shape[0], inp.num_kv_heads, inp.head_dim
+        g = torch.Generator().manual_seed(7)
+        k_new = torch.randn((T, H, D), generator=g).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((T, H, D), generator=g).to(torch.bfloat16).to(dev)
+        loc = new_token_slots(inp).to(dev)
+        kp, vp = inp.k_pool.to(dev), inp.v_pool.to(dev)
+        ks, vs = inp.meta["k_scale"], inp.meta["v_scale"]
+
+        def append():
+            b2pa.append_kv(k_new, v_new, (kp, vp), loc, ks, vs, inp.layout, stream=stream)
+
+        for _ in range(5):
+            append()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps)] for _ in range(2)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            flush.fill_(i)
+            ev[0][i].record(stream)
+            append()
+            ev[1][i].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in zip(ev[0], ev[1]))
+        esize = kp.element_size()
+        by = 2 * T * H * D * 2 + 2 * T * H * D * esize + 4 * T  # bf16 rows in, pool rows out, slots
+        print(json.dumps({"workload": f"append_kv:{inp.name}", "pool_dtype": str(kp.dtype).replace("torch.", ""),
+                          "tokens": T, "algorithmic_mb": by / 1e6, "kernel_ms": ms, "kernel_gbs": by / ms / 1e6,
+                          "frac_of_copy_peak": by / ms / 1e6 / hbm_gbs, "device_status": b2pa.device_status()}),
+              flush=True)
+
+
+def new_token_slots(inp):
+    """cache_loc of each request's new tokens (positions kv_len - q_len .. kv_len - 1) through its page table."""
+    P = inp.page_size
+    loc = []
+    for b in range(inp.batch):
+        q_len = int(inp.cum_q[b + 1] - inp.cum_q[b])
+        kv = int(inp.seq_lens[b])
+        pos = torch.arange(kv - q_len, kv)
+        loc.append(inp.block_tables[b].long()[pos // P] * P + pos % P)
+    return torch.cat(loc).to(torch.int32)
 
 
 def run_ours(args, world, rank, local):
@@ -570,7 +628,9 @@ def main():
     ap.add_argument("--cpu-fraction", type=float, default=0.125)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all-workloads", action="store_true",
-                    help="time every named workload (kernel and call) instead of the bench line")
+                    help="time every named workload (kernel and call) and the K/V writes instead of the bench line")
+    ap.add_argument("--append", action="store_true",
+                    help="time only the K/V writes (b2pa_append_kv) of the bench and ragged FP8 workloads")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K calls of the workload (for ncu); prints no measurement")
     args = ap.parse_args()
@@ -578,6 +638,9 @@ def main():
         args.warmup = 3
     if args.all_workloads:
         run_all_workloads()
+        return
+    if args.append:
+        run_append_workloads()
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

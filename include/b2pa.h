@@ -86,7 +86,9 @@ enum b2pa_device_error {
     B2PA_DEV_BAD_PAGE = 2,      /* a page id a request reads is outside [0, num_pages); those keys read as 0 */
     B2PA_DEV_TIMEOUT = 4,       /* a pipeline wait in a kernel gave up; the call's output is undefined */
     B2PA_DEV_BAD_CUM_KV = 8,    /* cum_kv[b+1] - cum_kv[b] != seq_lens[b] (checked only where cum_kv is read) */
-    B2PA_DEV_OVERFLOW = 16      /* more work items than the workspace holds (cannot happen for valid bounds) */
+    B2PA_DEV_OVERFLOW = 16,     /* more work items than the workspace holds (cannot happen for valid bounds) */
+    B2PA_DEV_BAD_SLOT = 32      /* b2pa_append_kv: a cache_loc entry outside [0, num_pages * page_size);
+                                   that token is not written */
 };
 
 /* Kernel paths (b2pa_set_kernel_path). */
@@ -215,6 +217,39 @@ B2PA_API int b2pa_debug_worklist(const b2pa_tensor* q, const b2pa_tensor* k_pool
 B2PA_API int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
                       const b2pa_tensor* seq_lens, const b2pa_tensor* cum_kv, int32_t layout,
                       b2pa_tensor* k_out, b2pa_tensor* v_out, b2pa_stream_t stream);
+
+/*
+ * b2pa_append_kv -- write new tokens' K and V into the paged pools: the step
+ * before the attention (TokenSpeed trtllm backend, _save_kv_and_prepare_q,
+ * which calls fused_fp8_set_kv_buffer(k, v, k_cache, v_cache, cache_loc,
+ * k_scale, v_scale, page_size) for an e4m3 cache and set_kv_buffer otherwise).
+ *
+ *   k_new, v_new     bf16 [T, Hkv, D] device tensors: token n's K and V rows.
+ *                    head_dim contiguous; token and head strides multiples of
+ *                    8 elements; 16-byte aligned; equal shapes and strides.
+ *   k_pool, v_pool   the pools and layout exactly as for b2pa_context_attention
+ *                    (bf16 or e4m3; Hkv and D must match k_new); their page,
+ *                    head and slot strides must be multiples of 8 elements and
+ *                    their bases 16-byte aligned.  Written in place.
+ *   cache_loc        int32 [T] device tensor: token n goes to page
+ *                    cache_loc[n] / page_size, slot cache_loc[n] % page_size.
+ *                    Slots should be distinct; where two tokens name one slot,
+ *                    which of them lands is unspecified.  A slot outside
+ *                    [0, num_pages * page_size) is skipped and sets
+ *                    B2PA_DEV_BAD_SLOT in the stream's device error word.
+ *   k_scale, v_scale used by an e4m3 pool only, which stores x / scale (one
+ *                    binary32 division) rounded to the nearest e4m3 value, ties
+ *                    to even, magnitudes above 448 saturating to 448; a bf16
+ *                    pool stores the bf16 bits unchanged.  Finite and > 0.
+ *   D must be a multiple of 8.  T = 0 is a no-op.
+ *
+ * Asynchronous on `stream`; the caller owns every buffer.  The pages print
+ * this call's interface, not its kernel; the rounding and saturation above
+ * are this library's reading.
+ */
+B2PA_API int b2pa_append_kv(const b2pa_tensor* k_new, const b2pa_tensor* v_new, const b2pa_tensor* k_pool,
+                            const b2pa_tensor* v_pool, const b2pa_tensor* cache_loc, float k_scale, float v_scale,
+                            int32_t layout, b2pa_stream_t stream);
 
 /*
  * b2pa_get_device_status -- synchronise `stream`, read and clear the device

@@ -42,6 +42,7 @@ EXPORTED = [
     "b2pa_context_attention_noalloc",
     "b2pa_debug_worklist",
     "b2pa_debug_gather",
+    "b2pa_append_kv",
     "b2pa_get_device_status",
     "b2pa_set_kernel_path",
     "b2pa_query_path",
@@ -94,6 +95,7 @@ def load(path: str = LIB_PATH):
     lib.b2pa_debug_worklist.restype = ctypes.c_int
     lib.b2pa_debug_gather.argtypes = [P, P, P, P, P, ctypes.c_int32, P, P, ctypes.c_void_p]
     lib.b2pa_debug_gather.restype = ctypes.c_int
+    lib.b2pa_append_kv.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_int32, ctypes.c_void_p]
     lib.b2pa_get_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     lib.b2pa_get_device_status.restype = ctypes.c_int
     lib.b2pa_set_kernel_path.argtypes = [ctypes.c_int32]
@@ -273,6 +275,22 @@ def debug_gather(kv_cache, block_tables, seq_lens, cum_seq_lens_kv, total_rows: 
                                ctypes.byref(dvo), ctypes.c_void_p(_stream_handle(stream)))
     _check(st, "b2pa_debug_gather")
     return k_out, v_out
+
+
+def append_kv(k_new: torch.Tensor, v_new: torch.Tensor, kv_cache, cache_loc: torch.Tensor, k_scale: float = 1.0,
+              v_scale: float = 1.0, kv_layout: str = "HND", stream=None):
+    """Write token n's K/V rows (bf16 [T, Hkv, D]) into slot cache_loc[n] (int32) of the pools, in place.
+
+    An e4m3 pool stores x / scale rounded to the nearest e4m3 value (saturating at +-448); a bf16
+    pool stores the values unchanged.  Slots outside the pool are skipped and flagged in
+    device_status().
+    """
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    d = [desc(x) for x in (k_new, v_new, k, v, cache_loc)]
+    st = lib.b2pa_append_kv(*(ctypes.byref(x) for x in d), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+                            LAYOUTS[kv_layout], ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "b2pa_append_kv")
 
 
 def device_status(stream=None) -> int:

@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "../../include/b2pa.h"
+#include "append.cuh"
 #include "common.cuh"
 
 using namespace b2pa;
@@ -685,6 +686,87 @@ int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, cons
     cudaError_t e = launch_gather(gp, pr.fp8, (int)(rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF), stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "gather launch");
+    return B2PA_OK;
+}
+
+int b2pa_append_kv(const b2pa_tensor* k_new, const b2pa_tensor* v_new, const b2pa_tensor* k_pool,
+                   const b2pa_tensor* v_pool, const b2pa_tensor* cache_loc, float k_scale, float v_scale,
+                   int32_t layout, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+    Problem pr;
+    std::memset(&pr, 0, sizeof pr);
+    int st = parse_pools(k_pool, v_pool, layout, &pr);
+    if (st)
+        return st;
+    if (!k_new || !v_new || k_new->ndim != 3 || v_new->ndim != 3 || k_new->dtype != B2PA_BF16 ||
+        v_new->dtype != B2PA_BF16)
+        return fail(B2PA_ERR_INVALID_ARG, "k_new / v_new must be bf16 [T, Hkv, D]");
+    const int64_t T = k_new->shape[0];
+    for (int i = 0; i < 3; ++i)
+        if (k_new->shape[i] != v_new->shape[i] || k_new->stride[i] != v_new->stride[i])
+            return fail(B2PA_ERR_INVALID_ARG, "k_new and v_new must have equal shapes and strides");
+    if (T < 0 || T > 0x7FFFFFFF || k_new->shape[1] != pr.Hkv || k_new->shape[2] != pr.D)
+        return fail(B2PA_ERR_INVALID_ARG, "k_new must be [T, Hkv, D] with the pools' Hkv and D (T < 2^31)");
+    if (pr.D % 8 != 0)
+        return fail(B2PA_ERR_UNSUPPORTED, "head_dim must be a multiple of 8");
+    if (!cache_loc || cache_loc->ndim != 1 || cache_loc->dtype != B2PA_INT32 || cache_loc->shape[0] != T)
+        return fail(B2PA_ERR_INVALID_ARG, "cache_loc must be int32 [T]");
+    if (pr.fp8 && (!std::isfinite(k_scale) || !(k_scale > 0.f) || !std::isfinite(v_scale) || !(v_scale > 0.f)))
+        return fail(B2PA_ERR_INVALID_ARG, "k_scale / v_scale must be finite and > 0");
+    if (T == 0)
+        return B2PA_OK;  // empty tensors may carry null data pointers
+    if (!k_new->data || !v_new->data)
+        return fail(B2PA_ERR_INVALID_ARG, "k_new / v_new: null data");
+    if ((pr.D > 1 && k_new->stride[2] != 1) || k_new->stride[0] % 8 != 0 || k_new->stride[1] % 8 != 0 ||
+        !aligned16(k_new->data) || !aligned16(v_new->data))
+        return fail(B2PA_ERR_INVALID_ARG,
+                    "k_new / v_new: head_dim contiguous, token and head strides multiples of 8, 16-byte aligned");
+    for (int i = 0; i < 3; ++i)
+        if (pr.k_st[i] % 8 != 0 || pr.v_st[i] % 8 != 0)
+            return fail(B2PA_ERR_INVALID_ARG, "pool page / head / slot strides must be multiples of 8 elements");
+    if (!aligned16(pr.k) || !aligned16(pr.v))
+        return fail(B2PA_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    if ((long long)pr.N * pr.P > 0x7FFFFFFFLL)
+        return fail(B2PA_ERR_UNSUPPORTED, "num_pages * page_size must be < 2^31 (int32 slots)");
+    if (!is_vec(cache_loc, B2PA_INT32, T))
+        return fail(B2PA_ERR_INVALID_ARG, "cache_loc must be contiguous int32 [T]");
+    int dev;
+    DevInfo di;
+    if ((st = device_info(&dev, &di)))
+        return st;
+    Workspace ws;
+    if ((st = get_workspace(dev, stream, 1, &ws)))
+        return st;
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof ap);
+    ap.k_new = static_cast<const uint16_t*>(k_new->data);
+    ap.v_new = static_cast<const uint16_t*>(v_new->data);
+    ap.new_st_tok = k_new->stride[0];
+    ap.new_st_head = k_new->stride[1];
+    ap.k_pool = const_cast<void*>(pr.k);
+    ap.v_pool = const_cast<void*>(pr.v);
+    for (int i = 0; i < 3; ++i) {
+        ap.k_st[i] = pr.k_st[i];
+        ap.v_st[i] = pr.v_st[i];
+    }
+    ap.cache_loc = static_cast<const int*>(cache_loc->data);
+    ap.T = (int)T;
+    ap.Hkv = pr.Hkv;
+    ap.D = pr.D;
+    ap.page_size = pr.P;
+    ap.num_pages = pr.N;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    ap.err = reinterpret_cast<unsigned*>(ws.mem);
+    // enough 256-thread blocks for every chunk, at most 8 per SM (grid-stride beyond)
+    const long long chunks = T * (long long)pr.Hkv * (pr.D / 8);
+    const long long want = (chunks + 255) / 256;
+    const int grid = (int)(want < 8LL * di.sms ? want : 8LL * di.sms);
+    cudaError_t e = launch_append(ap, pr.fp8, grid, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "append launch");
     return B2PA_OK;
 }
 

@@ -123,3 +123,41 @@ def test_binding_describes_torch_tensors():
     k, v = pkg.split_kv_cache(kv, "HND")
     assert k.shape == (5, 2, 16, 64) and k.stride(0) == 2 * 2 * 16 * 64
     assert v.data_ptr() - k.data_ptr() == 2 * 16 * 64
+
+
+def _append(lib, kn, vn, k, v, loc, ks=1.0, vs=1.0, layout=0):
+    r = ctypes.byref
+    return lib.b2pa_append_kv(r(kn), r(vn), r(k), r(v), r(loc), ks, vs, layout, None)
+
+
+def test_append_host_validation_without_gpu(lib):
+    BF, F8, F32, I32 = 1, 2, 3, 4
+    kn, vn = _fake([6, 2, 128], BF), _fake([6, 2, 128], BF)
+    k, v = _fake([10, 2, 32, 128], BF), _fake([10, 2, 32, 128], BF)
+    loc = _fake([6], I32)
+    # kv heads or head_dim differ from the pools
+    assert _append(lib, _fake([6, 3, 128], BF), _fake([6, 3, 128], BF), k, v, loc) == -1
+    assert _append(lib, _fake([6, 2, 64], BF), _fake([6, 2, 64], BF), k, v, loc) == -1
+    # new rows must be bf16, and K and V alike
+    assert _append(lib, _fake([6, 2, 128], F32), _fake([6, 2, 128], F32), k, v, loc) == -1
+    assert _append(lib, kn, _fake([7, 2, 128], BF), k, v, loc) == -1
+    # cache_loc: int32, one per token
+    assert _append(lib, kn, vn, k, v, _fake([5], I32)) == -1
+    assert _append(lib, kn, vn, k, v, _fake([6], F32)) == -1
+    # an e4m3 pool needs finite scales > 0
+    k8, v8 = _fake([10, 2, 32, 128], F8), _fake([10, 2, 32, 128], F8)
+    assert _append(lib, kn, vn, k8, v8, loc, ks=0.0) == -1
+    assert _append(lib, kn, vn, k8, v8, loc, vs=float("inf")) == -1
+    # token stride not a multiple of 8 elements
+    bk, bv = _fake([6, 2, 128], BF), _fake([6, 2, 128], BF)
+    bk.stride[0] = bv.stride[0] = 260
+    assert _append(lib, bk, bv, k, v, loc) == -1
+    # head_dim not a multiple of 8
+    assert _append(lib, _fake([6, 2, 12], BF), _fake([6, 2, 12], BF), _fake([10, 2, 32, 12], BF),
+                   _fake([10, 2, 32, 12], BF), loc) == -2
+    # no tokens: nothing to do, and no CUDA call; empty tensors may carry null data pointers
+    assert _append(lib, _fake([0, 2, 128], BF), _fake([0, 2, 128], BF), k, v, _fake([0], I32)) == 0
+    assert _append(lib, _fake([0, 2, 128], BF, base=0), _fake([0, 2, 128], BF, base=0), k, v,
+                   _fake([0], I32, base=0)) == 0
+    # but not when there are tokens
+    assert _append(lib, _fake([6, 2, 128], BF, base=0), vn, k, v, loc) == -1
