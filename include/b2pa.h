@@ -22,6 +22,10 @@
  * 内部", section "句柄到偏移的物理含义": the table holds page ids and the
  * kernel adds id x page stride to the pool base).
  *
+ * The library also does the step that precedes the attention in a serving
+ * engine: writing the new tokens' K and V into the pools (b2pa_append_kv,
+ * quantising to e4m3 for an FP8 cache).
+ *
  * Conventions for every entry point:
  *  - All tensors are described by b2pa_tensor: a pointer, a dtype, a rank,
  *    and shape/stride arrays in ELEMENTS.  Tensors are owned by the caller;
