@@ -7,6 +7,7 @@ import torch
 
 import oracle
 import workload
+from bench import new_token_slots
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -88,18 +89,6 @@ def test_append_of_no_tokens_is_a_no_op(cuda_lib):
     b2pa.append_kv(empty, empty, (dk, dv), torch.empty((0,), dtype=torch.int32, device=DEV))
     assert b2pa.device_status() == 0
     assert _same_bits(dk, kp) and _same_bits(dv, vp)
-
-
-def new_token_slots(inp):
-    """cache_loc of each request's new tokens: positions kv_len - q_len .. kv_len - 1, through its page table."""
-    P = inp.page_size
-    loc = []
-    for b in range(inp.batch):
-        q_len = int(inp.cum_q[b + 1] - inp.cum_q[b])
-        kv = int(inp.seq_lens[b])
-        pos = torch.arange(kv - q_len, kv)
-        loc.append(inp.block_tables[b].long()[pos // P] * P + pos % P)
-    return torch.cat(loc).to(torch.int32)
 
 
 def test_append_new_tokens_of_the_ragged_fp8_workload(cuda_lib):
