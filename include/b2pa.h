@@ -174,7 +174,8 @@ B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_p
  *                order.  b2pa_get_device_status does not see this entry
  *                point's errors.
  * Only the tensor-core path runs here: a shape it cannot take returns
- * B2PA_ERR_UNSUPPORTED (b2pa_query_path tells beforehand).
+ * B2PA_ERR_UNSUPPORTED (b2pa_query_path tells beforehand).  The timing events
+ * of b2pa_set_timing_events are not recorded by this entry point.
  *
  * The first call on a device looks up the scratch's device address there
  * (cudaGetSymbolAddress); make that first call before any stream capture.
@@ -275,7 +276,7 @@ B2PA_API int b2pa_query_path(const b2pa_tensor* q, const b2pa_tensor* k_pool, co
 B2PA_API int b2pa_set_debug_checks(int32_t on);
 
 /* Instrumentation (no counterpart on the pages): when both are non-NULL, later
- * b2pa_context_attention calls on the tensor-core path record start_event just
+ * b2pa_context_attention calls (that entry point only) on the tensor-core path record start_event just
  * before and stop_event just after launching the attention kernel, on the call's
  * stream, so a caller can time that kernel alone.  The arguments are cudaEvent_t
  * handles owned by the caller; NULL, NULL turns recording off. */

@@ -227,6 +227,12 @@ def context_attention_noalloc(
         if len(sinks) != 1:
             raise ValueError("sinks: one fp32 [num_heads] tensor")
         sinks = sinks[0]
+    if status is not None:
+        # the library writes 4 bytes there with a device-to-device copy
+        if (not status.is_cuda or status.device != query.device or status.dtype not in (torch.int32, torch.uint32)
+                or status.numel() < 1 or not status.is_contiguous()):
+            raise ValueError("status must be a contiguous int32/uint32 CUDA tensor of at least one element on "
+                             "the query's device")
     dq, dk, dv, dbt, dsl, dcq = (desc(x) for x in (query, k, v, block_tables, seq_lens, cum_seq_lens_q))
     dck, dsk, do = desc(cum_seq_lens_kv), desc(sinks), desc(out)
     st = lib.b2pa_context_attention_noalloc(

@@ -42,10 +42,14 @@
 // Every wait is bounded: after kWaitLimitNs (2 s of %globaltimer) the CTA raises
 // B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies and
 // MMAs are drained, and TMEM is freed before the CTA exits.
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
 namespace b2pa {
+
+constexpr int kItemRecWords = 10;  // a posted item: w, b, kvh, q0, q_len, kv_len, tok0, nq, n_lo, n_hi
 
 template <int D, bool FP8>
 struct TcCfg {
@@ -69,12 +73,18 @@ struct TcCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffRing = kOffQ + kQBufs * kQTiles * kQTileBytes;
     static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
-    static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
+    // output staging (16-bit KV paths; the e4m3 path has no room): per softmax
+    // warp, 32 rows x 64 columns of bf16, so that the output leaves in whole
+    // 128-byte lines instead of one 16-byte piece per row and instruction
+    static constexpr bool kStageOut = !FP8;
+    static constexpr int kStageWarpBytes = 32 * 128;
+    static constexpr int kOffStage = kOffF8 + kF8Stages * kF8TileBytes;
+    static constexpr int kOffBar = kOffStage + (kStageOut ? 8 * kStageWarpBytes : 0);
     // P_t is handed to the MMA warp in kPParts parts of kKvTile / kPParts keys
     static constexpr int kPParts = 1;
     static constexpr int kNumBars = (FP8 ? 3 : 2) * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
+    static constexpr int kSmemBytes = kOffMisc + 64 + kItemSlots * kItemRecWords * 4 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "fp8 path is D = 128");
     static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
@@ -156,16 +166,27 @@ __device__ __forceinline__ ItemInfo read_item(const AttnParams& p, int w)
     return r;
 }
 
-// The n-th item index of this CTA (-1: no more work), as posted by the producer.
+// The n-th item of this CTA (index -1: no more work) and its description, as
+// posted by the producer in shared memory (no global reads in the consumers).
 template <int kSlots>
-__device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint32_t n, bool* ok)
+__device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint32_t n, bool* ok, ItemInfo* it)
 {
     const uint32_t s = n % kSlots;
     if (!wait_bar(&c.bar.it_full[s], (n / kSlots) & 1, c.abort_flag, p.err)) {
         *ok = false;
         return -1;
     }
-    const int w = c.item_slot[s];
+    const volatile int* rec = c.item_slot + s * kItemRecWords;
+    const int w = rec[0];
+    it->b = rec[1];
+    it->kvh = rec[2];
+    it->q0 = rec[3];
+    it->q_len = rec[4];
+    it->kv_len = rec[5];
+    it->g.tok0 = rec[6];
+    it->g.nq = rec[7];
+    it->g.n_lo = rec[8];
+    it->g.n_hi = rec[9];
     __syncwarp();
     if ((threadIdx.x & 31) == 0)
         mbar_arrive(&c.bar.it_empty[s]);
@@ -201,18 +222,40 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         const uint32_t slot = n % C::kItemSlots;
         if (!wait_bar(&c.bar.it_empty[slot], ((n / C::kItemSlots) & 1) ^ 1, c.abort_flag, p.err))
             break;
-        int w = 0;
+        volatile int* rec = c.item_slot + slot * kItemRecWords;
         if (lane == 0) {
-            w = atomicAdd(p.counter, 1);
+            int w = atomicAdd(p.counter, 1);
             if (w >= c.n_items)
                 w = -1;
-            c.item_slot[slot] = w;
+            rec[0] = w;
+            if (w >= 0) {
+                const ItemInfo r = read_item(p, w);
+                rec[1] = r.b;
+                rec[2] = r.kvh;
+                rec[3] = r.q0;
+                rec[4] = r.q_len;
+                rec[5] = r.kv_len;
+                rec[6] = r.g.tok0;
+                rec[7] = r.g.nq;
+                rec[8] = r.g.n_lo;
+                rec[9] = r.g.n_hi;
+            }
             mbar_arrive(&c.bar.it_full[slot]);
         }
-        w = __shfl_sync(0xffffffffu, w, 0);
+        __syncwarp();
+        const int w = rec[0];
         if (w < 0)
             break;
-        const ItemInfo it = read_item(p, w);
+        ItemInfo it;
+        it.b = rec[1];
+        it.kvh = rec[2];
+        it.q0 = rec[3];
+        it.q_len = rec[4];
+        it.kv_len = rec[5];
+        it.g.tok0 = rec[6];
+        it.g.nq = rec[7];
+        it.g.n_lo = rec[8];
+        it.g.n_hi = rec[9];
         // Q tiles, into the buffer of this item once its previous user is done
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c.abort_flag, p.err))
@@ -359,8 +402,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
         uint32_t qb, first;
         bool ok;
     };
-    auto open_item = [&](int w, uint32_t n) -> Open {
-        const ItemInfo it = read_item(p, w);
+    auto open_item = [&](const ItemInfo& it, uint32_t n) -> Open {
         Open o;
         o.n_lo = it.g.n_lo;
         o.n_hi = it.g.n_hi;
@@ -386,9 +428,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     // its S_0 right after the last P_0 V, its S_1 after the last P_1 V, the
     // same order as between two kv tiles of one item.
     Open cur_item;
-    int w = take_item<C::kItemSlots>(p, c, 0, &ok);
+    ItemInfo info;
+    int w = take_item<C::kItemSlots>(p, c, 0, &ok, &info);
     if (w >= 0) {
-        cur_item = open_item(w, 0);
+        cur_item = open_item(info, 0);
         ok = cur_item.ok;
         for (int t = 0; ok && t < cur_item.nq; ++t)
             first_s(cur_item, t);
@@ -457,11 +500,11 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 } else if (t == (FP8 ? nq - 1 : 0)) {
                     // (FP8: after the last P V, since the next item's Q and K wait
                     // for the converter warps)
-                    w_next = take_item<C::kItemSlots>(p, c, n + 1, &ok);
+                    w_next = take_item<C::kItemSlots>(p, c, n + 1, &ok, &info);
                     if (!ok)
                         break;
                     if (w_next >= 0) {
-                        nxt = open_item(w_next, n + 1);
+                        nxt = open_item(info, n + 1);
                         if (!nxt.ok) {
                             ok = false;
                             break;
@@ -518,10 +561,10 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
-        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
+        ItemInfo it;
+        const int w = take_item<C::kItemSlots>(p, c, n, &ok, &it);
         if (w < 0)
             break;
-        const ItemInfo it = read_item(p, w);
         if (t >= it.g.nq)
             continue;
         const int prefix = it.kv_len - it.q_len;
@@ -686,23 +729,61 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         const float inv = (m_used != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
         const float2 inv2 = make_float2(inv, inv);
         uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
+        if constexpr (C::kStageOut) {
+            // each 64-column half of the warp's 32 rows goes through shared
+            // memory (row r in 128 bytes, 16-byte chunks swizzled by r % 8), then
+            // out with four whole rows per store instruction
+            const uint32_t stage = smem_u32(c.base + C::kOffStage + (t * 4 + wq) * C::kStageWarpBytes);
+            const unsigned long long my_row = reinterpret_cast<unsigned long long>(orow);
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
-            tmem_wait_ld();
-            if (valid) {
-                uint32_t pkd[16];
+            for (int hh = 0; hh < D / 64; ++hh) {
+                uint32_t oa[32], ob[32];
+                tmem_ld32(o_tmem + (uint32_t)(hh * 64), oa);
+                tmem_ld32(o_tmem + (uint32_t)(hh * 64 + 32), ob);
+                tmem_wait_ld();
+                uint32_t pk[32];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float2 v =
-                        __fmul2_rn(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), inv2);
-                    pkd[k] = pack_bf16x2(v.x, v.y);
+                    const float2 va = __fmul2_rn(make_float2(__uint_as_float(oa[2 * k]), __uint_as_float(oa[2 * k + 1])), inv2);
+                    const float2 vb = __fmul2_rn(make_float2(__uint_as_float(ob[2 * k]), __uint_as_float(ob[2 * k + 1])), inv2);
+                    pk[k] = pack_bf16x2(va.x, va.y);
+                    pk[16 + k] = pack_bf16x2(vb.x, vb.y);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
+                for (int cc = 0; cc < 8; ++cc)
+                    st_shared_v4(stage + (uint32_t)(lane * 128 + ((cc ^ (lane & 7)) << 4)), pk[4 * cc], pk[4 * cc + 1],
+                                 pk[4 * cc + 2], pk[4 * cc + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = 4 * k + (lane >> 3), cc = lane & 7;
+                    const uint4 v = ld_shared_v4(stage + (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4)));
+                    const unsigned long long a = __shfl_sync(0xffffffffu, my_row, r);
+                    const int vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
+                    if (vr)
+                        *reinterpret_cast<uint4*>(a + (unsigned long long)(hh * 128 + cc * 16)) = v;
+                }
+                __syncwarp();
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
+                tmem_wait_ld();
+                if (valid) {
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float2 v =
+                            __fmul2_rn(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), inv2);
+                        pkd[k] = pack_bf16x2(v.x, v.y);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
+                }
             }
         }
     }
@@ -739,10 +820,10 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
     uint32_t r8 = 0, r = 0;
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
-        const int w = take_item<C::kItemSlots>(p, c, n, &ok);
+        ItemInfo it;
+        const int w = take_item<C::kItemSlots>(p, c, n, &ok, &it);
         if (w < 0)
             break;
-        const ItemInfo it = read_item(p, w);
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
@@ -918,9 +999,9 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             convert_role<D, FP8>(p, c);
         }
     } else {
-        // 384 threads launch with 168 registers each (96 + 200 + 200 = 496 <= 3 x 168)
+        // 384 threads launch with 168 registers each (104 + 200 + 200 = 504 = 3 x 168)
         if (warp < 4) {
-            regs_dec<96>();
+            regs_dec<104>();
             if (warp == 0)
                 producer_role<D, FP8>(p, c);
             else if (warp == 1)
@@ -945,14 +1026,19 @@ static cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream
     using C = TcCfg<D, FP8>;
     auto kern = attention_tc_kernel<D, FP8>;
     int dev = 0;
-    cudaGetDevice(&dev);
-    static unsigned long long attr_done = 0;  // one bit per device
-    if (dev < 64 && !(attr_done & (1ull << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done |= 1ull << dev;
-    }
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    // the shared-memory opt-in, once per device and instantiation (any host thread)
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    std::call_once(attr_once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    });
+    if (attr_err[dev] != cudaSuccess)
+        return attr_err[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::kThreads);

@@ -474,12 +474,12 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         AttnParams ap;
         std::memset(&ap, 0, sizeof ap);
         const int rpt = rows_per_tile_of(pr);
+        // a shape the tensor-core path accepts must encode; a failure is an
+        // error of the call, never a silent switch to the other kernel
         if ((st = encode_q_map(&ap.tm_q, pr, rpt)) || (st = encode_pool_map(&ap.tm_k, pr, pr.k, pr.k_st)) ||
-            (st = encode_pool_map(&ap.tm_v, pr, pr.v, pr.v_st))) {
-            if (g_path.load() == B2PA_PATH_TCGEN05)
-                return st;
-            use_tc = false;  // fall through to the generic path
-        } else {
+            (st = encode_pool_map(&ap.tm_v, pr, pr.v, pr.v_st)))
+            return st;
+        {
             SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
             cudaError_t e = launch_schedule(sp, stream);
             if (e != cudaSuccess)

@@ -1,5 +1,7 @@
 // sched_gather.cu -- the work-list scheduler of the tensor-core path and the
 // debug gather that exercises its paged K/V loads.
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -207,9 +209,22 @@ cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
 {
     const size_t nb = (size_t)p.nbuckets;
     const size_t smem = sizeof(int) * (32 * nb + 64 + nb + 3 * (size_t)p.B + 1);
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    // opt in once per device to the most shared memory any call can need
+    // (every bucket in use and the largest batch), not on every call
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    std::call_once(attr_once[dev], [&] {
+        const size_t most = sizeof(int) * (32 * (size_t)kSchedBuckets + 64 + kSchedBuckets + 3 * (size_t)kSchedMaxBatch + 1);
+        attr_err[dev] = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    });
+    if (attr_err[dev] != cudaSuccess)
+        return attr_err[dev];
     schedule_kernel<<<1, kSchedThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }

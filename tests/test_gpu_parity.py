@@ -4,6 +4,29 @@ Bars for bf16 outputs on N(0,1) inputs:
 max-abs <= 2e-2 and mean-abs <= 2e-3; FP8 KV: max-abs <= 3e-2 against the
 oracle fed the same e4m3 values and scales.  Integer work (gathered K/V and
 the work list) must match bit for bit.
+
+Those absolute bars alone are loose on long rows: with N(0,1) inputs the
+softmax of a row with n visible keys is nearly flat and its output is an
+average of order 1/sqrt(n) (about 0.03 on the Llama-3-8B-shaped prefill), so
+a lost or doubled K/V tile could stay under 2e-2.  Two things make the
+comparison bind there:
+
+* every case also runs "sharp", with q scaled by 4 before its bf16 rounding,
+  which peaks the softmax and lifts outputs to order 1.  Its q is no longer
+  N(0,1), and an output near a single V value reaches |o| of 4 to 5, where
+  half a bf16 ulp alone is 2^-6 = 0.0156; so the sharp runs take their
+  elementwise bar from the same arithmetic instead of the fixed 2e-2:
+  |e| <= 2^-8 (|o_ref| + bmm2 max|V|), twice the sum of the output rounding
+  (2^-9 |o|) and the P rounding (2^-9 sum_j p_j |V_j| / l <= 2^-9 bmm2 max|V|);
+* each row must also meet a relative bar, ||o - o_ref|| / ||o_ref|| <= 1e-2
+  over its head_dim elements.  The arithmetic fixes the expected value: the
+  bf16 output and the bf16 (f16 on the e4m3 path) P each round with a
+  relative error of at most 2^-9, independent from element to element, so a
+  row's relative L2 error is about 2^-9 (2e-3); 1e-2 leaves a factor of five,
+  while a dropped tile of a row with t tiles gives about 1/t.
+
+Every assertion message reports max-abs, mean-abs, the largest elementwise
+relative error |e| / max(|o_ref|, 1e-3) and the largest row-relative error.
 """
 import math
 
@@ -17,6 +40,8 @@ import workload
 pytestmark = pytest.mark.gpu
 
 TOL_MAX, TOL_MEAN, TOL_MAX_FP8 = 2e-2, 2e-3, 3e-2
+TOL_ROW_REL = 1e-2
+Q_SCALES = [1.0, 4.0]
 DEV = "cuda:0"
 
 
@@ -43,6 +68,18 @@ def _run(b2pa, inp, path="auto", out=None, dev=None):
     return out, bits
 
 
+def _errors(g, ref):
+    """max-abs, mean-abs, max elementwise relative, max row-relative L2 error of g vs ref ([rows, D] float64)."""
+    err = (g - ref).abs()
+    rel = (err / ref.abs().clamp_min(1e-3)).max().item()
+    ref_norm = ref.norm(dim=1)
+    live = ref_norm > 0  # rows with no visible key are exactly 0 in the oracle
+    row_rel = (err.norm(dim=1)[live] / ref_norm[live]).max().item() if live.any() else 0.0
+    if (~live).any():
+        row_rel = max(row_rel, err[~live].max().item())
+    return err.max().item(), err.mean().item(), rel, row_rel
+
+
 def _compare(got, inp, rows=None, fp8=None):
     """got: [T, H, D] device tensor.  rows: None = all, else int64 token*H+h."""
     fp8 = inp.meta.get("kv_dtype") == "fp8_e4m3" if fp8 is None else fp8
@@ -52,13 +89,23 @@ def _compare(got, inp, rows=None, fp8=None):
     g = got.float().cpu().reshape(T * H, D).double()
     if rows is not None:
         g = g[torch.as_tensor(rows)]
-    err = (g - torch.from_numpy(ref)).abs()
     assert torch.isfinite(g).all(), "non-finite output"
-    mx, mean = err.max().item(), err.mean().item()
-    if fp8:
-        assert mx <= TOL_MAX_FP8, (mx, mean)
+    ref = torch.from_numpy(ref)
+    mx, mean, rel, row_rel = _errors(g, ref)
+    msg = (f"{inp.name}: max_abs={mx:.3e} mean_abs={mean:.3e} max_rel={rel:.3e} max_row_rel={row_rel:.3e} "
+           f"rows={g.shape[0]}")
+    print(msg)
+    if inp.meta.get("q_scale", 1.0) != 1.0:
+        vmax = inp.v_pool.float().abs().nan_to_num(0.0).max().item() * abs(inp.bmm2_scale)
+        bar = 2.0 ** -8 * (ref.abs() + vmax)
+        worst = ((g - ref).abs() / bar).max().item()
+        assert worst <= 1.0, f"{msg} elementwise error / derived bar = {worst:.3f}"
+        assert mean <= TOL_MEAN, msg
+    elif fp8:
+        assert mx <= TOL_MAX_FP8, msg
     else:
-        assert mx <= TOL_MAX and mean <= TOL_MEAN, (mx, mean)
+        assert mx <= TOL_MAX and mean <= TOL_MEAN, msg
+    assert row_rel <= TOL_ROW_REL, msg
     return mx, mean
 
 
@@ -82,11 +129,12 @@ TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("q_scale", Q_SCALES)
 @pytest.mark.parametrize("case", range(len(TC_CASES)))
-def test_tcgen05_parity_small(cuda_lib, case):
+def test_tcgen05_parity_small(cuda_lib, case, q_scale):
     ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = TC_CASES[case]
     inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=100 + case,
-                         table_pad="garbage")
+                         table_pad="garbage", q_scale=q_scale)
     assert cuda_lib.query_path(inp.q.to(DEV), (inp.k_pool.to(DEV), inp.v_pool.to(DEV)), kv_layout=lay) == "tcgen05"
     out, bits = _run(cuda_lib, inp, "tcgen05")
     assert bits == 0
@@ -131,10 +179,12 @@ def test_scheduler_batch_limit(cuda_lib):
     _compare(out2, inp2)
 
 
+@pytest.mark.parametrize("q_scale", Q_SCALES)
 @pytest.mark.parametrize("case", range(len(TC_CASES)))
-def test_generic_parity_small(cuda_lib, case):
+def test_generic_parity_small(cuda_lib, case, q_scale):
     ql, kl, H, Hkv, D, P, lay, W, sinks, kvd = TC_CASES[case]
-    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=100 + case)
+    inp = workload.build(ql, kl, H, Hkv, D, P, lay, kv_dtype=kvd, window_left=W, with_sinks=sinks, seed=100 + case,
+                         q_scale=q_scale)
     out, bits = _run(cuda_lib, inp, "generic")
     assert bits == 0
     _compare(out, inp)
@@ -187,12 +237,20 @@ def _sample_rows(inp, n_random, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
+# Every row of the bench workload and of the sliding-window layer is compared
+# (the oracle does them in seconds on the host cores); the chunked-prefix, full
+# D = 64 and ragged FP8 workloads on every request's boundary rows plus 4000
+# random rows.
+FULL_ROWS = {(2, None), (4, None)}
+
+
+@pytest.mark.parametrize("q_scale", Q_SCALES)
 @pytest.mark.parametrize("index,window", [(2, None), (3, None), (4, None), (4, -1), (5, None)])
-def test_named_workloads_sampled(cuda_lib, index, window):
-    inp = workload.config(index, window_left=window)
+def test_named_workloads(cuda_lib, index, window, q_scale):
+    inp = workload.config(index, window_left=window, q_scale=q_scale)
     out, bits = _run(cuda_lib, inp)
     assert bits == 0
-    rows = _sample_rows(inp, 600, seed=index)
+    rows = None if (index, window) in FULL_ROWS else _sample_rows(inp, 4000, seed=index)
     _compare(out, inp, rows=rows)
     # properties that hold at any size: finite everywhere, and every row of a
     # valid request was written (the NaN fill is gone)

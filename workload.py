@@ -239,7 +239,8 @@ def build(
         layout=layout,
         name=name,
         seed=seed,
-        meta={"k_scale": k_scale, "v_scale": v_scale, "kv_dtype": kv_dtype, "pool_pages": n_pages},
+        meta={"k_scale": k_scale, "v_scale": v_scale, "kv_dtype": kv_dtype, "pool_pages": n_pages,
+              "q_scale": q_scale},
     )
 
 
@@ -262,7 +263,7 @@ def _uniform_int(gen, lo, hi, n):
     return torch.randint(lo, hi + 1, (n,), generator=gen).tolist()
 
 
-def config(index: int, window_left: Optional[int] = None, seed: Optional[int] = None) -> Inputs:
+def config(index: int, window_left: Optional[int] = None, seed: Optional[int] = None, q_scale: float = 1.0) -> Inputs:
     """The named workloads 1..5.
 
     1: batch 2, q_lens [5,3], kv_lens [9,3], H 2 / Hkv 1, D 16, P 4, HND, pool
@@ -273,31 +274,35 @@ def config(index: int, window_left: Optional[int] = None, seed: Optional[int] = 
        fp32 sinks ~ N(0,1); ``window_left=-1`` gives its full-attention layer.
     5: batch 32, q log-uniform [1, 4096], prefix ~ U[0, 28672], H 32 / Hkv 8,
        D 128, P 32, HND, K/V e4m3 with per-tensor scales.
+
+    ``q_scale`` multiplies q before its bf16 rounding (the "sharp" variant:
+    q x 4 makes the softmax peaked, so that outputs of long rows are no longer
+    averages near zero); every other draw is unchanged.
     """
     s = 1234 + index if seed is None else seed
     g = torch.Generator().manual_seed(s)
-    name = CONFIG_NAMES[index]
+    name = CONFIG_NAMES[index] + ("" if q_scale == 1.0 else f"_qx{q_scale:g}")
     if index == 1:
         # 9 + 3 tokens need 3 + 1 pages of an 8-page pool.
         inp = build([5, 3], [9, 3], 2, 1, 16, 4, "HND", pool_factor=1.0, extra_pages=4,
-                    max_pages=3, seed=s, name=name)
+                    max_pages=3, seed=s, name=name, q_scale=q_scale)
         return inp
     if index == 2:
         L = _uniform_int(g, 512, 2048, 8)
-        return build(L, L, 32, 8, 128, 32, "HND", pool_factor=2.0, seed=s, name=name)
+        return build(L, L, 32, 8, 128, 32, "HND", pool_factor=2.0, seed=s, name=name, q_scale=q_scale)
     if index == 3:
         K = _uniform_int(g, 1024, 8192, 16)
-        return build([512] * 16, K, 64, 8, 128, 64, "NHD", pool_factor=2.0, seed=s, name=name)
+        return build([512] * 16, K, 64, 8, 128, 64, "NHD", pool_factor=2.0, seed=s, name=name, q_scale=q_scale)
     if index == 4:
         W = 127 if window_left is None else window_left
         nm = name if W == 127 else name.replace("swa127", f"swa{W}" if W >= 0 else "full")
         return build([4096] * 4, [4096] * 4, 64, 8, 64, 16, "HND", window_left=W, with_sinks=True,
-                     pool_factor=2.0, seed=s, name=nm)
+                     pool_factor=2.0, seed=s, name=nm, q_scale=q_scale)
     if index == 5:
         u = torch.rand((32,), generator=g, dtype=torch.float64) * math.log(4096.0)
         ql = [min(4096, max(1, int(round(math.exp(x))))) for x in u.tolist()]
         pre = _uniform_int(g, 0, 28672, 32)
         kv = [a + b for a, b in zip(ql, pre)]
         return build(ql, kv, 32, 8, 128, 32, "HND", kv_dtype="fp8_e4m3", pool_factor=2.0,
-                     seed=s, name=name)
+                     seed=s, name=name, q_scale=q_scale)
     raise ValueError(index)
