@@ -497,9 +497,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     mma_commit_p(&c.bar.s_full[t], issue);
                     if (t == nq - 1 && j + 1 == n_hi)
                         mma_commit_p(&c.bar.q_empty[qb], issue);
-                } else if (t == (FP8 ? nq - 1 : 0)) {
-                    // (FP8: after the last P V, since the next item's Q and K wait
-                    // for the converter warps)
+                } else if (t == (D == 128 ? nq - 1 : 0)) {
+                    // D = 128 (and FP8): after the item's last P V of both tiles, so
+                    // neither tile's epilogue waits behind the next item's start
+                    // (measured faster there); D = 64: right after the last P_0 V
                     w_next = take_item<C::kItemSlots>(p, c, n + 1, &ok, &info);
                     if (!ok)
                         break;
@@ -510,10 +511,10 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                             break;
                         }
                         first_s(nxt, 0);
-                        if ((FP8 || nq == 1) && nxt.nq > 1)
+                        if ((D == 128 || nq == 1) && nxt.nq > 1)
                             first_s(nxt, 1);  // no P_1 V left to wait for in this item
                     }
-                } else if (!FP8 && w_next >= 0 && nxt.nq > 1) {
+                } else if (D != 128 && w_next >= 0 && nxt.nq > 1) {
                     first_s(nxt, 1);
                 }
             }
@@ -731,12 +732,21 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
         if constexpr (C::kStageOut) {
             // each 64-column half of the warp's 32 rows goes through shared
-            // memory (row r in 128 bytes, 16-byte chunks swizzled by r % 8), then
-            // out with four whole rows per store instruction
+            // memory (row r in 128 bytes, 16-byte chunks swizzled by r % 8: the
+            // 128-byte swizzle of the output tensor map).  When all 32 rows are
+            // written and form whole boxes, lane 0 sends them with one TMA store
+            // (asynchronous; nothing else waits for it); otherwise the warp
+            // copies them out itself, four whole rows per store instruction.
             const uint32_t stage = smem_u32(c.base + C::kOffStage + (t * 4 + wq) * C::kStageWarpBytes);
             const unsigned long long my_row = reinterpret_cast<unsigned long long>(orow);
+            const bool by_tma = p.out_tma != 0 && __all_sync(0xffffffffu, valid);
+            const int r0 = wq * 32;  // first row of the warp: token r0 / G, head r0 % G
+            const int c1 = it.kvh * G + r0 % G, c2 = it.q0 + i_first + r0 / G;
 #pragma unroll
             for (int hh = 0; hh < D / 64; ++hh) {
+                if (lane == 0)
+                    bulk_wait_read_all();  // the previous store has read the staging
+                __syncwarp();
                 uint32_t oa[32], ob[32];
                 tmem_ld32(o_tmem + (uint32_t)(hh * 64), oa);
                 tmem_ld32(o_tmem + (uint32_t)(hh * 64 + 32), ob);
@@ -753,17 +763,26 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                 for (int cc = 0; cc < 8; ++cc)
                     st_shared_v4(stage + (uint32_t)(lane * 128 + ((cc ^ (lane & 7)) << 4)), pk[4 * cc], pk[4 * cc + 1],
                                  pk[4 * cc + 2], pk[4 * cc + 3]);
-                __syncwarp();
+                if (by_tma) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&p.tm_o, stage, hh * 64, c1, c2);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int r = 4 * k + (lane >> 3), cc = lane & 7;
-                    const uint4 v = ld_shared_v4(stage + (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4)));
-                    const unsigned long long a = __shfl_sync(0xffffffffu, my_row, r);
-                    const int vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
-                    if (vr)
-                        *reinterpret_cast<uint4*>(a + (unsigned long long)(hh * 128 + cc * 16)) = v;
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = 4 * k + (lane >> 3), cc = lane & 7;
+                        const uint4 v = ld_shared_v4(stage + (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4)));
+                        const unsigned long long a = __shfl_sync(0xffffffffu, my_row, r);
+                        const int vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
+                        if (vr)
+                            *reinterpret_cast<uint4*>(a + (unsigned long long)(hh * 128 + cc * 16)) = v;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         } else {
 #pragma unroll
@@ -787,6 +806,8 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             }
         }
     }
+    if (C::kStageOut && lane == 0)
+        bulk_wait_all();  // this warp's output stores are complete before the CTA exits
     tc_fence_before();
 }
 
@@ -954,6 +975,8 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         prefetch_tmap(&p.tm_q);
         prefetch_tmap(&p.tm_k);
         prefetch_tmap(&p.tm_v);
+        if (p.out_tma)
+            prefetch_tmap(&p.tm_o);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, C::kTmemCols);

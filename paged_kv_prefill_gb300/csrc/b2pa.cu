@@ -376,7 +376,73 @@ int encode_q_map(CUtensorMap* m, const Problem& pr, int rows_per_tile)
     return B2PA_OK;
 }
 
+// The output as a 3-D (D, H, T) map whose box is one softmax warp's 32 rows
+// (64 columns at a time): {64, min(G, 32), max(1, 32 / G)}.  Only when 32
+// rows are whole boxes (G divides 32 or 32 divides G); *ok = false otherwise or
+// if the driver rejects the map, and the kernel then stores the rows itself.
+int encode_o_map(CUtensorMap* m, const Problem& pr, bool* ok)
+{
+    *ok = false;
+    EncodeTiledFn fn = encode_fn();
+    const int G = pr.H / pr.Hkv;
+    if (!fn || !(32 % G == 0 || G % 32 == 0))
+        return B2PA_OK;
+    long long s_head = pr.out_st_head * 2, s_tok = pr.out_st_tok * 2;
+    if (pr.H == 1)
+        s_head = (long long)pr.D * 2;
+    if (pr.T <= 1)
+        s_tok = s_head * pr.H;
+    cuuint64_t dims[3] = {(cuuint64_t)pr.D, (cuuint64_t)pr.H, (cuuint64_t)(pr.T > 0 ? pr.T : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)s_head, (cuuint64_t)s_tok};
+    cuuint32_t box[3] = {64, (cuuint32_t)(G < 32 ? G : 32), (cuuint32_t)(G < 32 ? 32 / G : 1)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pr.out, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *ok = r == CUDA_SUCCESS;
+    return B2PA_OK;
+}
+
 int rows_per_tile_of(const Problem& pr) { return kQRows / (pr.H / pr.Hkv); }
+
+// Everything the tensor-core kernel takes: tensor maps, pointers, geometry and
+// scales; the work list and counters come from the scheduler's parameters.
+int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, size_t cap, int window,
+                     float bmm1_scale, float bmm2_scale)
+{
+    std::memset(ap, 0, sizeof *ap);
+    const int rpt = rows_per_tile_of(pr);
+    int st;
+    if ((st = encode_q_map(&ap->tm_q, pr, rpt)) || (st = encode_pool_map(&ap->tm_k, pr, pr.k, pr.k_st)) ||
+        (st = encode_pool_map(&ap->tm_v, pr, pr.v, pr.v_st)))
+        return st;
+    bool o_ok = false;
+    encode_o_map(&ap->tm_o, pr, &o_ok);
+    ap->out_tma = o_ok ? 1 : 0;
+    ap->cum_q = pr.cum_q;
+    ap->seq_lens = pr.seq;
+    ap->block_tables = pr.bt;
+    ap->sinks = pr.sinks;
+    ap->out = static_cast<uint16_t*>(pr.out);
+    ap->bt_stride = pr.bt_stride;
+    ap->out_stride_tok = pr.out_st_tok;
+    ap->out_stride_head = pr.out_st_head;
+    ap->items = sp.items;
+    ap->count = sp.count;
+    ap->counter = sp.counter;
+    ap->err = sp.err;
+    ap->cap = (int)cap;
+    ap->H = pr.H;
+    ap->Hkv = pr.Hkv;
+    ap->G = pr.H / pr.Hkv;
+    ap->rows_per_tile = rpt;
+    ap->page_size = pr.P;
+    ap->num_pages = pr.N;
+    ap->window = window;
+    ap->scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
+    ap->bmm2 = bmm2_scale;
+    return B2PA_OK;
+}
 
 size_t items_needed(const Problem& pr, int max_q_len)
 {
@@ -464,60 +530,31 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     bool use_tc = false;
     if ((st = choose_path(pr, di, &use_tc)))
         return st;
-    const float scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
-
     if (use_tc) {
         const size_t cap = items_needed(pr, max_q_len);
         Workspace ws;
         if ((st = get_workspace(dev, stream, cap, &ws)))
             return st;
+        SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
         AttnParams ap;
-        std::memset(&ap, 0, sizeof ap);
-        const int rpt = rows_per_tile_of(pr);
         // a shape the tensor-core path accepts must encode; a failure is an
         // error of the call, never a silent switch to the other kernel
-        if ((st = encode_q_map(&ap.tm_q, pr, rpt)) || (st = encode_pool_map(&ap.tm_k, pr, pr.k, pr.k_st)) ||
-            (st = encode_pool_map(&ap.tm_v, pr, pr.v, pr.v_st)))
+        if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale)))
             return st;
-        {
-            SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
-            cudaError_t e = launch_schedule(sp, stream);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "scheduler launch");
-            ap.cum_q = pr.cum_q;
-            ap.seq_lens = pr.seq;
-            ap.block_tables = pr.bt;
-            ap.sinks = pr.sinks;
-            ap.out = static_cast<uint16_t*>(pr.out);
-            ap.bt_stride = pr.bt_stride;
-            ap.out_stride_tok = pr.out_st_tok;
-            ap.out_stride_head = pr.out_st_head;
-            ap.items = sp.items;
-            ap.count = sp.count;
-            ap.counter = sp.counter;
-            ap.err = sp.err;
-            ap.cap = (int)cap;
-            ap.H = pr.H;
-            ap.Hkv = pr.Hkv;
-            ap.G = pr.H / pr.Hkv;
-            ap.rows_per_tile = rpt;
-            ap.page_size = pr.P;
-            ap.num_pages = pr.N;
-            ap.window = window;
-            ap.scale_log2 = scale_log2;
-            ap.bmm2 = bmm2_scale;
-            cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_ev_start.load());
-            cudaEvent_t ev1 = static_cast<cudaEvent_t>(g_ev_stop.load());
-            const bool timed = ev0 != nullptr && ev1 != nullptr;
-            if (timed && (e = cudaEventRecord(ev0, stream)) != cudaSuccess)
-                return cuda_fail(e, "cudaEventRecord");
-            e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, !timed);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "attention kernel launch");
-            if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
-                return cuda_fail(e, "cudaEventRecord");
-            return B2PA_OK;
-        }
+        cudaError_t e = launch_schedule(sp, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "scheduler launch");
+        cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_ev_start.load());
+        cudaEvent_t ev1 = static_cast<cudaEvent_t>(g_ev_stop.load());
+        const bool timed = ev0 != nullptr && ev1 != nullptr;
+        if (timed && (e = cudaEventRecord(ev0, stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, !timed);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "attention kernel launch");
+        if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        return B2PA_OK;
     }
     Workspace ws;
     if ((st = get_workspace(dev, stream, 1, &ws)))
@@ -554,7 +591,7 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     gp.max_q_len = max_q_len;
     gp.max_kv_len = max_kv_len;
     gp.window = window;
-    gp.scale_log2 = scale_log2;
+    gp.scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
     gp.bmm2 = bmm2_scale;
     gp.err = reinterpret_cast<unsigned*>(ws.mem);
     cudaError_t e = launch_attention_generic(gp, pr.fp8, stream);
@@ -971,43 +1008,17 @@ int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_tensor* k_po
     if ((st = noalloc_scratch(dev, &mem)))
         return st;
     const Workspace ws{dev, stream, mem, kNoAllocBytes};
-
+    const int window = window_left < 0 ? -1 : window_left;
+    SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
     AttnParams ap;
-    std::memset(&ap, 0, sizeof ap);
-    const int rpt = rows_per_tile_of(pr);
-    if ((st = encode_q_map(&ap.tm_q, pr, rpt)) || (st = encode_pool_map(&ap.tm_k, pr, pr.k, pr.k_st)) ||
-        (st = encode_pool_map(&ap.tm_v, pr, pr.v, pr.v_st)))
+    if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale)))
         return st;
     // the error word must start at zero (the scheduler resets the work counter itself)
     cudaError_t e = cudaMemsetAsync(mem, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(error word)");
-    const int window = window_left < 0 ? -1 : window_left;
-    SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
     if ((e = launch_schedule(sp, stream)) != cudaSuccess)
         return cuda_fail(e, "scheduler launch");
-    ap.cum_q = pr.cum_q;
-    ap.seq_lens = pr.seq;
-    ap.block_tables = pr.bt;
-    ap.sinks = pr.sinks;
-    ap.out = static_cast<uint16_t*>(pr.out);
-    ap.bt_stride = pr.bt_stride;
-    ap.out_stride_tok = pr.out_st_tok;
-    ap.out_stride_head = pr.out_st_head;
-    ap.items = sp.items;
-    ap.count = sp.count;
-    ap.counter = sp.counter;
-    ap.err = sp.err;
-    ap.cap = (int)cap;
-    ap.H = pr.H;
-    ap.Hkv = pr.Hkv;
-    ap.G = pr.H / pr.Hkv;
-    ap.rows_per_tile = rpt;
-    ap.page_size = pr.P;
-    ap.num_pages = pr.N;
-    ap.window = window;
-    ap.scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
-    ap.bmm2 = bmm2_scale;
     if ((e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true)) != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");
     if (dev_status && (e = cudaMemcpyAsync(dev_status, mem, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream)) !=

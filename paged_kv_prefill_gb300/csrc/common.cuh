@@ -88,6 +88,8 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     CUtensorMap tm_q;   // 3-D: (D, H, T), box (64, G, rows_per_tile)
     CUtensorMap tm_k;   // 4-D: (D, P, Hkv, pages), box (64 | 128 bytes, min(P,128), 1, 1)
     CUtensorMap tm_v;
+    CUtensorMap tm_o;   // 3-D: (D, H, T), box (64, min(G, 32), max(1, 32 / G)): one warp's 32 rows
+    int out_tma;        // 1: tm_o is valid and a warp's 32 rows are whole boxes (G divides 32 or 32 divides G)
     const int* cum_q;
     const int* seq_lens;
     const int* block_tables;
