@@ -16,7 +16,7 @@ constexpr int kQTiles = 2;        // query tiles per work item (they share every
 constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
-constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 3 ints per request in shared memory
+constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 5 words per request in shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait that exceeds this gives up
 
 // A request is processed only if its lengths are consistent with the bounds
@@ -59,7 +59,8 @@ __device__ __forceinline__ ItemGeom item_geometry(int q_len, int kv_len, int it,
     const int per_item = rows_per_tile * kQTiles;
     g.tok0 = it * per_item;
     int i1 = min(g.tok0 + per_item, q_len) - 1;
-    g.nq = (i1 - g.tok0) / rows_per_tile + 1;
+    static_assert(kQTiles == 2, "query tiles per item");
+    g.nq = i1 - g.tok0 >= rows_per_tile ? 2 : 1;  // (i1 - tok0) / rows_per_tile + 1, without a division
     int prefix = kv_len - q_len;
     int p_min = prefix + g.tok0, p_max = prefix + i1;
     int lo = window < 0 ? 0 : max(0, p_min - window);

@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     int* req_start = tot + nb;                       // [B + 1] first item of each request
     int* req_q = req_start + B + 1;                  // [B] q_len
     int* req_kv = req_q + B;                         // [B] kv_len
+    int* req_nit = req_kv + B;                       // [B] items per kv head
+    float* req_inv = reinterpret_cast<float*>(req_nit + B);  // [B] 1 / items per kv head
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per_item = p.rows_per_tile * kQTiles;
     if (tid == 0)
@@ -88,6 +90,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         req_start[b] = n;  // count for now
         req_q[b] = r.q_len;
         req_kv[b] = r.kv_len;
+        const int n_it = (r.q_len + per_item - 1) / per_item;
+        req_nit[b] = n_it;
+        req_inv[b] = n_it > 0 ? 1.0f / (float)n_it : 0.f;
         local += n;
         if (p.debug) {
             if (p.cum_kv != nullptr && r.ok && p.cum_kv[b + 1] - p.cum_kv[b] != r.kv_len)
@@ -131,9 +136,15 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         const int b = lo;
         const int q_len = req_q[b];
         const int kv_len = req_kv[b];
-        const int n_it = (q_len + per_item - 1) / per_item;
+        const int n_it = req_nit[b];
         const int loc = idx - req_start[b];
-        const int kvh = loc / n_it, it = loc % n_it;
+        // kvh = loc / n_it from the float reciprocal, corrected to the exact quotient
+        int kvh = (int)((float)loc * req_inv[b]);
+        while (kvh > 0 && kvh * n_it > loc)
+            --kvh;
+        while ((kvh + 1) * n_it <= loc)
+            ++kvh;
+        const int it = loc - kvh * n_it;
         const ItemGeom g = item_geometry(q_len, kv_len, it, p.rows_per_tile, p.window);
         const int cost = (g.n_hi - g.n_lo + 1) * g.nq;
         item = make_int4(b, kvh, it, cost);
@@ -144,17 +155,34 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     const int s_begin = min(n_total, warp * seg), s_end = min(n_total, s_begin + seg);
     int* my_hist = hist + warp * nb;
 
-    // 2. per-warp bucket counts
-    for (int base = s_begin; base < s_end; base += 32) {
+    // 2. per-warp bucket counts.  The first kKeep rounds of 32 items stay in
+    // registers for the scatter; later rounds are decoded again there.
+    constexpr int kKeep = 4;
+    int4 kept_item[kKeep];
+    int kept_bucket[kKeep];
+    auto count_round = [&](int bucket) {
+        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
+        if (bucket >= 0 && lane == __ffs(grp) - 1)
+            my_hist[bucket] += __popc(grp);
+        __syncwarp();
+    };
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k) {
+        const int idx = s_begin + 32 * k + lane;
+        kept_item[k] = make_int4(0, 0, 0, 0);
+        kept_bucket[k] = -1;
+        if (idx < s_end)
+            decode(idx, kept_item[k], kept_bucket[k]);
+        if (s_begin + 32 * k < s_end)  // warp-uniform
+            count_round(kept_bucket[k]);
+    }
+    for (int base = s_begin + 32 * kKeep; base < s_end; base += 32) {
         const int idx = base + lane;
         int4 item;
         int bucket = -1;
         if (idx < s_end)
             decode(idx, item, bucket);
-        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
-        if (bucket >= 0 && lane == __ffs(grp) - 1)
-            my_hist[bucket] += __popc(grp);
-        __syncwarp();
+        count_round(bucket);
     }
     __syncthreads();
 
@@ -182,13 +210,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         tot[nb - 1 - tid] = start;
     __syncthreads();
 
-    // 4. scatter
-    for (int base = s_begin; base < s_end; base += 32) {
-        const int idx = base + lane;
-        int4 item = make_int4(0, 0, 0, 0);
-        int bucket = -1;
-        if (idx < s_end)
-            decode(idx, item, bucket);
+    // 4. scatter, in the same order as the counts
+    auto scatter_round = [&](const int4& item, int bucket) {
         const unsigned grp = __match_any_sync(0xffffffffu, bucket);
         const unsigned lower = grp & ((1u << lane) - 1u);
         if (bucket >= 0) {
@@ -200,6 +223,18 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
         if (bucket >= 0 && lane == __ffs(grp) - 1)
             my_hist[bucket] += __popc(grp);
         __syncwarp();
+    };
+#pragma unroll
+    for (int k = 0; k < kKeep; ++k)
+        if (s_begin + 32 * k < s_end)  // warp-uniform
+            scatter_round(kept_item[k], kept_bucket[k]);
+    for (int base = s_begin + 32 * kKeep; base < s_end; base += 32) {
+        const int idx = base + lane;
+        int4 item = make_int4(0, 0, 0, 0);
+        int bucket = -1;
+        if (idx < s_end)
+            decode(idx, item, bucket);
+        scatter_round(item, bucket);
     }
     if (tid == 0)
         *p.count = n_total;
@@ -208,7 +243,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
 {
     const size_t nb = (size_t)p.nbuckets;
-    const size_t smem = sizeof(int) * (32 * nb + 64 + nb + 3 * (size_t)p.B + 1);
+    const size_t smem = sizeof(int) * (32 * nb + 64 + nb + 5 * (size_t)p.B + 1);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -220,7 +255,7 @@ cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     std::call_once(attr_once[dev], [&] {
-        const size_t most = sizeof(int) * (32 * (size_t)kSchedBuckets + 64 + kSchedBuckets + 3 * (size_t)kSchedMaxBatch + 1);
+        const size_t most = sizeof(int) * (32 * (size_t)kSchedBuckets + 64 + kSchedBuckets + 5 * (size_t)kSchedMaxBatch + 1);
         attr_err[dev] = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     });
     if (attr_err[dev] != cudaSuccess)
