@@ -17,9 +17,13 @@
 //                 buffered across items where shared memory allows) and of
 //                 K/V pages (4-D map, one box per page and 128-byte column
 //                 block) through a ring that holds K and V of a kv tile side
-//                 by side under one full and one empty mbarrier (FP8: the
-//                 converters signal K and V separately), so each tile costs
-//                 the MMA warp one wait and one release.
+//                 by side.  At head_dim 128 (16-bit KV), whose ring holds only
+//                 two tiles, K and V land and are released separately: a K
+//                 entry is free once the tile's last Q K^T has completed, one
+//                 softmax earlier than its V, so the next K is fetched that
+//                 much sooner.  Elsewhere a tile's K and V are released
+//                 together after its last P V (one barrier less per tile;
+//                 measured faster there).
 //   warp 1        MMA issuer (one lane): S_t = Q_t K^T into TMEM, then
 //                 O_t += P_t V with P_t read from TMEM, for t = 0, 1, in the
 //                 order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) so the tensor
@@ -63,6 +67,7 @@ struct TcCfg {
     static constexpr int kQBufs = D == 128 ? 1 : 2;                 // Q buffers (items in flight)
     static constexpr int kStages = D == 128 ? 4 : 8;                // 16-bit ring entries
     static constexpr int kPairs = kStages / 2;                      // tiles in the ring
+    static constexpr bool kSplitKV = D == 128 && !FP8;              // K and V released separately
     static constexpr int kF8Stages = FP8 ? 2 : 0;                   // e4m3 staging ring
     static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
     static constexpr int kThreads = FP8 ? 512 : 384;
@@ -82,7 +87,7 @@ struct TcCfg {
     static constexpr int kOffBar = kOffStage + (kStageOut ? 8 * kStageWarpBytes : 0);
     // P_t is handed to the MMA warp in kPParts parts of kKvTile / kPParts keys
     static constexpr int kPParts = 1;
-    static constexpr int kNumBars = (FP8 ? 3 : 2) * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
+    static constexpr int kNumBars = 4 * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + kItemSlots * kItemRecWords * 4 + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
@@ -92,9 +97,10 @@ struct TcCfg {
 };
 
 struct Bars {
-    uint64_t* full;      // [kPairs]   16-bit K and V of a kv tile landed (TMA bytes, or converter warps)
-    uint64_t* empty;     // [kPairs]   K and V of the tile consumed by the MMAs
-    uint64_t* vfull;     // [kPairs]   (FP8) V of the tile converted; full then means K alone
+    uint64_t* full;      // [kPairs]   16-bit K of a kv tile landed (merged release: K and V)
+    uint64_t* empty;     // [kPairs]   K of the tile consumed, its last Q K^T done (merged: K and V, last P V)
+    uint64_t* vfull;     // [kPairs]   16-bit V of the tile landed (split release and FP8)
+    uint64_t* vempty;    // [kPairs]   V of the tile consumed, its last P V done (split release)
     uint64_t* f8full;    // [kF8Stages]
     uint64_t* f8empty;   // [kF8Stages]
     uint64_t* q_full;    // [kQBufs]   Q tiles landed
@@ -216,6 +222,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     const uint32_t q_box_bytes = (uint32_t)(p.G * p.rows_per_tile * 128);
 
     uint32_t ring_idx = 0;
+    uint32_t ring_kv[2] = {0, 0};  // 16-bit path: K and V tiles whose copies were started
     bool ok = true;
     for (uint32_t n = 0; ok; ++n) {
         // post the next item index
@@ -281,23 +288,32 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
             const uint32_t bytes = nvalid * (uint32_t)box_rows * 128u * kBoxes;
             if constexpr (!FP8) {
-                // K and V of the tile into one ring pair, under one barrier
+                // K into ring entry 2m, V into 2m + 1: with the split release each
+                // once its previous K (or V) is consumed, under its own barrier;
+                // otherwise both once the pair is free, under one barrier
                 const uint32_t m = ring_idx % C::kPairs, ph = (ring_idx / C::kPairs) & 1;
-                if (!wait_bar(&c.bar.empty[m], ph ^ 1, c.abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                // predicated rather than branched: the warp stays converged
-                mbar_arrive_expect_tx_p(&c.bar.full[m], 2 * bytes, lane == 0 ? 1u : 0u);
-                __syncwarp();
 #pragma unroll
                 for (int kind = 0; kind < 2; ++kind) {
+                    const bool own = C::kSplitKV || kind == 0;  // this kind waits and posts its bytes
+                    uint64_t* fb = (C::kSplitKV && kind) ? &c.bar.vfull[m] : &c.bar.full[m];
+                    if (own && !wait_bar((C::kSplitKV && kind) ? &c.bar.vempty[m] : &c.bar.empty[m], ph ^ 1,
+                                         c.abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    // predicated rather than branched: the warp stays converged
+                    if (own)
+                        mbar_arrive_expect_tx_p(fb, C::kSplitKV ? bytes : 2 * bytes, lane == 0 ? 1u : 0u);
+                    __syncwarp();
                     const uint32_t dst = ring + (2 * m + kind) * kRingTileBytes + (uint32_t)(lane * box_rows * 128);
 #pragma unroll
                     for (int h = 0; h < kBoxes; ++h)
-                        tma_load_4d_p(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, &c.bar.full[m], h * 64, slot0,
-                                      it.kvh, page, valid ? 1u : 0u);
+                        tma_load_4d_p(dst + h * C::kHalfBytes, kind ? &p.tm_v : &p.tm_k, fb, h * 64, slot0, it.kvh,
+                                      page, valid ? 1u : 0u);
+                    ++ring_kv[kind];
                 }
+                if (!ok)
+                    break;
                 ++ring_idx;
             } else {
                 for (int kind = 0; kind < 2; ++kind) {
@@ -323,11 +339,19 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     }
     if (*c.abort_flag) {
         // let the copies this warp started land before the CTA releases its memory
-        // (16-bit KV: ring_idx counts tiles, one barrier per pair; FP8: e4m3 entries)
-        constexpr int kSlots = FP8 ? kRingStages : C::kPairs;
-        const uint32_t first = ring_idx > (uint32_t)kSlots ? ring_idx - kSlots : 0;
-        for (uint32_t k = first; k < ring_idx; ++k)
-            drain_wait(&rfull[k % kSlots], (k / kSlots) & 1);
+        if constexpr (FP8) {
+            const uint32_t first = ring_idx > (uint32_t)kRingStages ? ring_idx - kRingStages : 0;
+            for (uint32_t k = first; k < ring_idx; ++k)
+                drain_wait(&rfull[k % kRingStages], (k / kRingStages) & 1);
+        } else {
+            for (int kind = 0; kind < 2; ++kind) {
+                uint64_t* fb = (C::kSplitKV && kind) ? c.bar.vfull : c.bar.full;
+                const uint32_t n_kv = C::kSplitKV || kind == 0 ? ring_kv[kind] : 0;
+                const uint32_t first = n_kv > (uint32_t)C::kPairs ? n_kv - C::kPairs : 0;
+                for (uint32_t k = first; k < n_kv; ++k)
+                    drain_wait(&fb[k % C::kPairs], (k / C::kPairs) & 1);
+            }
+        }
     }
 }
 
@@ -420,8 +444,12 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     auto first_s = [&](const Open o, int t) {
         issue_s(o.qb, t, k_slot(o.first));
         mma_commit_p(&c.bar.s_full[t], issue);
-        if (t == o.nq - 1 && o.n_lo == o.n_hi)
-            mma_commit_p(&c.bar.q_empty[o.qb], issue);
+        if (t == o.nq - 1) {
+            if (C::kSplitKV)
+                mma_commit_p(&empty[o.first % C::kPairs], issue);  // K of the tile consumed
+            if (o.n_lo == o.n_hi)
+                mma_commit_p(&c.bar.q_empty[o.qb], issue);
+        }
     };
 
     // The next item is opened while the current one's last kv tile finishes:
@@ -446,7 +474,8 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
         for (int j = n_lo; ok && j <= n_hi; ++j) {
             const bool last = j == n_hi;
             const uint32_t next = last ? 0u : ring_idx++;
-            if (FP8 && !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c.abort_flag, p.err)) {
+            if ((FP8 || C::kSplitKV) &&
+                !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c.abort_flag, p.err)) {
                 ok = false;
                 break;
             }
@@ -482,8 +511,8 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 if (!ok)
                     break;
                 ++p_cnt[t];
-                if (t == nq - 1)
-                    mma_commit_p(&empty[cur % C::kPairs], issue);  // K and V of tile j consumed
+                if (t == nq - 1)  // V of tile j consumed (merged release: K and V)
+                    mma_commit_p(C::kSplitKV ? &c.bar.vempty[cur % C::kPairs] : &empty[cur % C::kPairs], issue);
                 if (last)
                     mma_commit_p(&c.bar.o_full[t], issue);
                 if (!last) {
@@ -495,8 +524,12 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                     }
                     issue_s(qb, t, k_slot(next));
                     mma_commit_p(&c.bar.s_full[t], issue);
-                    if (t == nq - 1 && j + 1 == n_hi)
-                        mma_commit_p(&c.bar.q_empty[qb], issue);
+                    if (t == nq - 1) {
+                        if (C::kSplitKV)
+                            mma_commit_p(&empty[next % C::kPairs], issue);  // K of tile j + 1 consumed
+                        if (j + 1 == n_hi)
+                            mma_commit_p(&c.bar.q_empty[qb], issue);
+                    }
                 } else if (t == (D == 128 ? nq - 1 : 0)) {
                     // D = 128 (and FP8): after the item's last P V of both tiles, so
                     // neither tile's epilogue waits behind the next item's start
@@ -925,7 +958,8 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     c.bar.full = bars;
     c.bar.empty = c.bar.full + C::kPairs;
     c.bar.vfull = c.bar.empty + C::kPairs;
-    c.bar.f8full = c.bar.vfull + (FP8 ? C::kPairs : 0);
+    c.bar.vempty = c.bar.vfull + C::kPairs;
+    c.bar.f8full = c.bar.vempty + C::kPairs;
     c.bar.f8empty = c.bar.f8full + C::kF8Stages;
     c.bar.q_full = c.bar.f8empty + C::kF8Stages;
     c.bar.q_empty = c.bar.q_full + C::kQBufs;
@@ -945,8 +979,8 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         for (int s = 0; s < C::kPairs; ++s) {
             mbar_init(&c.bar.full[s], FP8 ? 4 : 1);
             mbar_init(&c.bar.empty[s], 1);
-            if (FP8)
-                mbar_init(&c.bar.vfull[s], 4);
+            mbar_init(&c.bar.vfull[s], FP8 ? 4 : 1);
+            mbar_init(&c.bar.vempty[s], 1);
         }
         for (int s = 0; s < C::kF8Stages; ++s) {
             mbar_init(&c.bar.f8full[s], 1);
