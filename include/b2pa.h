@@ -91,8 +91,10 @@ enum b2pa_device_error {
     B2PA_DEV_TIMEOUT = 4,       /* a pipeline wait in a kernel gave up; the call's output is undefined */
     B2PA_DEV_BAD_CUM_KV = 8,    /* cum_kv[b+1] - cum_kv[b] != seq_lens[b] (checked only where cum_kv is read) */
     B2PA_DEV_OVERFLOW = 16,     /* more work items than the workspace holds (cannot happen for valid bounds) */
-    B2PA_DEV_BAD_SLOT = 32      /* b2pa_append_kv: a cache_loc entry outside [0, num_pages * page_size);
+    B2PA_DEV_BAD_SLOT = 32,     /* b2pa_append_kv: a cache_loc entry outside [0, num_pages * page_size);
                                    that token is not written */
+    B2PA_DEV_BAD_SCALE = 64     /* b2pa_context_attention_tensor_scales: the device bmm1_scale is not
+                                   finite and > 0, or bmm2_scale is not finite; nothing is written */
 };
 
 /* Kernel paths (b2pa_set_kernel_path). */
@@ -146,6 +148,33 @@ B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_p
                            int32_t max_kv_len, float bmm1_scale, float bmm2_scale, int32_t window_left,
                            const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out,
                            b2pa_stream_t stream);
+
+/*
+ * b2pa_context_attention_tensor_scales -- b2pa_context_attention with
+ * bmm1_scale and bmm2_scale given as device tensors instead of host floats.
+ * The FlashInfer API reference types both as "float | Tensor": a serving
+ * engine that computes its FP8 scales on the GPU (k_scale, v_scale folded in,
+ * as the TokenSpeed backend's _compute_scales does) passes them without a
+ * device-to-host copy and without synchronising.
+ *
+ *  bmm1_scale, bmm2_scale   fp32 device tensors of one element (ndim 0 or 1),
+ *                           4-byte aligned, read by the kernels in stream
+ *                           order.  bmm1_scale * log2(e) is formed in double
+ *                           and rounded once, exactly as the host-float entry
+ *                           point does, so both give identical outputs for
+ *                           identical scale values.
+ * Every other argument, the layout rules and the errors are those of
+ * b2pa_context_attention.  A device bmm1_scale that is not finite and > 0, or
+ * a bmm2_scale that is not finite, cannot be seen on the host: the kernels
+ * then write nothing and set B2PA_DEV_BAD_SCALE in the stream's device error
+ * word.
+ */
+B2PA_API int b2pa_context_attention_tensor_scales(const b2pa_tensor* q, const b2pa_tensor* k_pool,
+                           const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
+                           const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q, const b2pa_tensor* cum_kv,
+                           int32_t max_q_len, int32_t max_kv_len, const b2pa_tensor* bmm1_scale,
+                           const b2pa_tensor* bmm2_scale, int32_t window_left, const b2pa_tensor* sinks,
+                           int32_t layout, b2pa_tensor* out, b2pa_stream_t stream);
 
 /*
  * b2pa_context_attention_noalloc -- the same attention, for callers that must

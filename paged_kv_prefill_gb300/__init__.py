@@ -29,6 +29,7 @@ PATH_AUTO, PATH_TCGEN05, PATH_GENERIC = 0, 1, 2
 STATUS = {0: "B2PA_OK", -1: "B2PA_ERR_INVALID_ARG", -2: "B2PA_ERR_UNSUPPORTED", -3: "B2PA_ERR_CUDA",
           -4: "B2PA_ERR_DEVICE"}
 DEV_BAD_REQUEST, DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_CUM_KV, DEV_OVERFLOW = 1, 2, 4, 8, 16
+DEV_BAD_SLOT, DEV_BAD_SCALE = 32, 64
 
 _DTYPES = {
     torch.bfloat16: B2PA_BF16,
@@ -39,6 +40,7 @@ _DTYPES = {
 
 EXPORTED = [
     "b2pa_context_attention",
+    "b2pa_context_attention_tensor_scales",
     "b2pa_context_attention_noalloc",
     "b2pa_debug_worklist",
     "b2pa_debug_gather",
@@ -85,6 +87,9 @@ def load(path: str = LIB_PATH):
     lib.b2pa_context_attention.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                            ctypes.c_float, ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
     lib.b2pa_context_attention.restype = ctypes.c_int
+    lib.b2pa_context_attention_tensor_scales.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P,
+                                                         ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
+    lib.b2pa_context_attention_tensor_scales.restype = ctypes.c_int
     lib.b2pa_context_attention_noalloc.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, ctypes.c_int32, P,
                                                    ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_void_p]
@@ -169,8 +174,8 @@ def context_attention(
     seq_lens: torch.Tensor,
     max_q_len: int,
     max_kv_len: int,
-    bmm1_scale: float,
-    bmm2_scale: float,
+    bmm1_scale: Union[float, torch.Tensor],
+    bmm2_scale: Union[float, torch.Tensor],
     cum_seq_lens_q: torch.Tensor,
     cum_seq_lens_kv: Optional[torch.Tensor] = None,
     window_left: int = -1,
@@ -179,7 +184,10 @@ def context_attention(
     sinks: Optional[torch.Tensor] = None,
     stream=None,
 ) -> torch.Tensor:
-    """Batched context attention over a paged KV cache (see include/b2pa.h)."""
+    """Batched context attention over a paged KV cache (see include/b2pa.h).
+
+    bmm1_scale / bmm2_scale are floats, or one-element fp32 device tensors (then
+    both must be tensors and b2pa_context_attention_tensor_scales is called)."""
     lib = load()
     k, v = split_kv_cache(kv_cache, kv_layout)
     if out is None:
@@ -190,6 +198,17 @@ def context_attention(
         sinks = sinks[0]
     dq, dk, dv, dbt, dsl, dcq = (desc(x) for x in (query, k, v, block_tables, seq_lens, cum_seq_lens_q))
     dck, dsk, do = desc(cum_seq_lens_kv), desc(sinks), desc(out)
+    if isinstance(bmm1_scale, torch.Tensor) or isinstance(bmm2_scale, torch.Tensor):
+        if not (isinstance(bmm1_scale, torch.Tensor) and isinstance(bmm2_scale, torch.Tensor)):
+            raise TypeError("bmm1_scale and bmm2_scale must both be floats or both be tensors")
+        d1, d2 = desc(bmm1_scale), desc(bmm2_scale)
+        st = lib.b2pa_context_attention_tensor_scales(
+            ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dbt), ctypes.byref(dsl),
+            ctypes.byref(dcq), _ref(dck), int(max_q_len), int(max_kv_len), ctypes.byref(d1), ctypes.byref(d2),
+            int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
+        )
+        _check(st, "b2pa_context_attention_tensor_scales")
+        return out
     st = lib.b2pa_context_attention(
         ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dbt), ctypes.byref(dsl),
         ctypes.byref(dcq), _ref(dck), int(max_q_len), int(max_kv_len), float(bmm1_scale), float(bmm2_scale),

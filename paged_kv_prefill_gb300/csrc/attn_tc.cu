@@ -33,7 +33,9 @@
 //                 and the epilogue (bmm2_scale / denominator, bf16 stores).
 //   warps 8-11    the same for query tile 1.
 //   warps 12-15   (FP8 KV only) convert e4m3 K/V tiles to f16 in the MMA
-//                 layout, and the Q tile from bf16 to f16.
+//                 layout (exact), and each Q row from bf16 to f16 after
+//                 scaling it by a power of two into f16's range (exact); the
+//                 softmax divides that power of two out of the row's scale.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // P_t (16-bit, two per column) overwrites the first 64 columns of S_t and is
@@ -89,7 +91,12 @@ struct TcCfg {
     static constexpr int kPParts = 1;
     static constexpr int kNumBars = 4 * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 64 + kItemSlots * kItemRecWords * 4 + 1024;  // + slack to align the base to 1024
+    // FP8: the power-of-two exponent of each Q row (int8), for the items of
+    // both parities (a row's exponent is read by the softmax while the next
+    // item's Q is being converted)
+    static constexpr int kOffQExp = kOffMisc + 64 + kItemSlots * kItemRecWords * 4;
+    static constexpr int kQExpBytes = FP8 ? 2 * kQTiles * kQRows : 0;
+    static constexpr int kSmemBytes = kOffQExp + kQExpBytes + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "fp8 path is D = 128");
     static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
@@ -105,7 +112,7 @@ struct Bars {
     uint64_t* f8empty;   // [kF8Stages]
     uint64_t* q_full;    // [kQBufs]   Q tiles landed
     uint64_t* q_empty;   // [kQBufs]   last Q K^T of the item done
-    uint64_t* q_conv;    // [kQBufs]   (FP8) Q converted to f16
+    uint64_t* q_conv;    // [kQBufs]   (FP8) Q rows scaled and converted to f16, their exponents posted
     uint64_t* s_full;    // [2]        S_t in TMEM
     uint64_t* p_full;    // [2][kPParts] part h of P_t in TMEM (4 softmax warps)
     uint64_t* o_full;    // [2]        last P V of the item done
@@ -224,6 +231,11 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     uint32_t ring_idx = 0;
     uint32_t ring_kv[2] = {0, 0};  // 16-bit path: K and V tiles whose copies were started
     bool ok = true;
+    // scales passed as device tensors are checked here: if they are unusable,
+    // no item is taken, so every role finishes without writing anything
+    const bool scales_ok = load_scales(p.scale_log2, p.bmm2, p.bmm1_dev, p.bmm2_dev).ok;
+    if (!scales_ok && blockIdx.x == 0 && lane == 0)
+        atomicOr(p.err, (unsigned)B2PA_DEV_BAD_SCALE);
     for (uint32_t n = 0; ok; ++n) {
         // post the next item index
         const uint32_t slot = n % C::kItemSlots;
@@ -231,7 +243,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             break;
         volatile int* rec = c.item_slot + slot * kItemRecWords;
         if (lane == 0) {
-            int w = atomicAdd(p.counter, 1);
+            int w = scales_ok ? atomicAdd(p.counter, 1) : -1;
             if (w >= c.n_items)
                 w = -1;
             rec[0] = w;
@@ -590,7 +602,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
     const int G = p.G, Tq = p.rows_per_tile;
     const int r_tok = row / G, r_head = row % G;
     const bool row_real = row < G * Tq;
-    const float sl2 = p.scale_log2;
+    const Scales scl = load_scales(p.scale_log2, p.bmm2, p.bmm1_dev, p.bmm2_dev);
 
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
@@ -599,8 +611,21 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         const int w = take_item<C::kItemSlots>(p, c, n, &ok, &it);
         if (w < 0)
             break;
+        // FP8: every item's Q conversion is awaited (also by a warpgroup with no
+        // query tile in it: a waiter that skipped phases could mistake a later
+        // one for an earlier one); the row's Q was scaled by 2^k before its
+        // conversion to f16, so its scores carry 2^k, taken out here
+        if (FP8 && !wait_bar(&c.bar.q_conv[n % C::kQBufs], (n / C::kQBufs) & 1, c.abort_flag, p.err)) {
+            ok = false;
+            break;
+        }
         if (t >= it.g.nq)
             continue;
+        float sl2 = scl.scale_log2;
+        if constexpr (FP8) {
+            const int k = reinterpret_cast<const int8_t*>(c.base + C::kOffQExp)[(n & 1) * kQTiles * kQRows + t * kQRows + row];
+            sl2 *= __int_as_float((127 - k) << 23);
+        }
         const int prefix = it.kv_len - it.q_len;
         const int i_first = it.g.tok0 + t * Tq;
         const int i = i_first + r_tok;
@@ -760,7 +785,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         float total = l;
         if (p.sinks != nullptr && m_used != -INFINITY && row_real)
             total += ex2_approx(fmaf(p.sinks[h], kLog2e, -m_used));
-        const float inv = (m_used != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
+        const float inv = (m_used != -INFINITY && total > 0.f) ? scl.bmm2 / total : 0.f;
         const float2 inv2 = make_float2(inv, inv);
         uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
         if constexpr (C::kStageOut) {
@@ -847,22 +872,30 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 // ---------------------------------------------------------------------------
 // e4m3 -> f16 conversion (FP8 KV path): warps 12-15, one thread per tile row.
 // ---------------------------------------------------------------------------
+// Two e4m3 values (low 16 bits of `two`) to two f16: exact, since every
+// e4m3 value (subnormals included) is a normal f16 or zero.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
 {
     uint32_t r;
-    const uint16_t h = (uint16_t)two;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+    const uint16_t in = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(in));
     return r;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+// Power-of-two exponent k that brings a Q row with largest magnitude `mx`
+// (bf16 bits, sign cleared) to [2^14, 2^15): then every element of the row at
+// least 2^-31 of the largest is an exact f16 after scaling by 2^k (a bf16
+// value has 8 significant bits, an f16 11, and f16 is exact down to 2^-17 at
+// that precision).  Clamped to [-30, 100] so that 2^k and 2^-k stay normal
+// floats; 0 for an all-zero row.
+__device__ __forceinline__ int q_row_exponent(uint32_t mx)
 {
-    const float lo = __uint_as_float(w << 16);
-    const float hi = __uint_as_float(w & 0xFFFF0000u);
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
+    if (mx == 0)
+        return 0;
+    const int e = (int)((mx >> 7) & 0xFFu) - 127;  // unbiased exponent of the largest element
+    return min(100, max(-30, 14 - e));
 }
+
 
 template <int D, bool FP8>
 __device__ void convert_role(const AttnParams& p, const Ctx& c)
@@ -878,19 +911,39 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
         const int w = take_item<C::kItemSlots>(p, c, n, &ok, &it);
         if (w < 0)
             break;
+        // Q: thread ct takes row ct of each query tile: scale by 2^k into f16's
+        // range, convert in place (same swizzled positions), post k
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_full[qb], qph, c.abort_flag, p.err))
             break;
+        int8_t* qexp = reinterpret_cast<int8_t*>(c.base + C::kOffQExp) + (n & 1) * kQTiles * kQRows;
         for (int t = 0; t < it.g.nq; ++t) {
-            uint4* q = reinterpret_cast<uint4*>(c.base + C::kOffQ + (qb * kQTiles + t) * C::kQTileBytes);
-            for (int k = ct; k < C::kQTileBytes / 16; k += 128) {
-                uint4 v = q[k];
-                v.x = bf16x2_to_f16x2(v.x);
-                v.y = bf16x2_to_f16x2(v.y);
-                v.z = bf16x2_to_f16x2(v.z);
-                v.w = bf16x2_to_f16x2(v.w);
-                q[k] = v;
-            }
+            uint8_t* qrow = c.base + C::kOffQ + (qb * kQTiles + t) * C::kQTileBytes + ct * 128;
+            uint32_t mx = 0;  // largest magnitude of the row, as bf16 bits
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + h * C::kHalfBytes + (q << 4));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        mx = max(mx, max(w4[e] & 0x7FFFu, (w4[e] >> 16) & 0x7FFFu));
+                }
+            const int k = q_row_exponent(mx);
+            const float sc = __int_as_float((127 + k) << 23);
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + h * C::kHalfBytes + (q << 4));
+                    uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w4[e] << 16) * sc, hi = __uint_as_float(w4[e] & 0xFFFF0000u) * sc;
+                        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w4[e]) : "f"(hi), "f"(lo));
+                    }
+                    *reinterpret_cast<uint4*>(qrow + h * C::kHalfBytes + (q << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            qexp[t * kQRows + ct] = (int8_t)k;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -1041,9 +1094,9 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
 
     if constexpr (FP8) {
         // 512 threads launch with 128 registers each; the softmax warpgroups
-        // take registers from the others (96 + 176 + 176 + 64 = 512 = 4 x 128)
+        // take registers from the others (88 + 176 + 176 + 72 = 512 = 4 x 128)
         if (warp < 4) {
-            regs_dec<96>();
+            regs_dec<88>();
             if (warp == 0)
                 producer_role<D, FP8>(p, c);
             else if (warp == 1)
@@ -1052,7 +1105,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
             regs_inc<176>();
             softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
         } else {
-            regs_dec<64>();
+            regs_dec<72>();
             convert_role<D, FP8>(p, c);
         }
     } else {

@@ -408,7 +408,8 @@ int rows_per_tile_of(const Problem& pr) { return kQRows / (pr.H / pr.Hkv); }
 // Everything the tensor-core kernel takes: tensor maps, pointers, geometry and
 // scales; the work list and counters come from the scheduler's parameters.
 int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, size_t cap, int window,
-                     float bmm1_scale, float bmm2_scale)
+                     float bmm1_scale, float bmm2_scale, const float* bmm1_dev = nullptr,
+                     const float* bmm2_dev = nullptr)
 {
     std::memset(ap, 0, sizeof *ap);
     const int rpt = rows_per_tile_of(pr);
@@ -441,7 +442,24 @@ int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, s
     ap->window = window;
     ap->scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
     ap->bmm2 = bmm2_scale;
+    ap->bmm1_dev = bmm1_dev;
+    ap->bmm2_dev = bmm2_dev;
     return B2PA_OK;
+}
+
+// A one-element fp32 device tensor holding a scale (the FlashInfer API's
+// "float | Tensor" bmm scales); its pointer, or nullptr with an error set.
+const float* scale_tensor(const b2pa_tensor* t, const char* what)
+{
+    if (!t || !t->data || t->dtype != B2PA_FP32 || t->ndim < 0 || t->ndim > 1 || (t->ndim == 1 && t->shape[0] != 1)) {
+        fail(B2PA_ERR_INVALID_ARG, "%s must be a one-element fp32 device tensor", what);
+        return nullptr;
+    }
+    if ((reinterpret_cast<uintptr_t>(t->data) & 3u) != 0) {
+        fail(B2PA_ERR_INVALID_ARG, "%s must be 4-byte aligned", what);
+        return nullptr;
+    }
+    return static_cast<const float*>(t->data);
 }
 
 size_t items_needed(const Problem& pr, int max_q_len)
@@ -498,20 +516,14 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     return sp;
 }
 
-}  // namespace
-
-// ====================================================================== C ABI
-
-extern "C" {
-
-int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+// Both attention entry points: scales as host floats, or (bmm1_dev, bmm2_dev
+// non-null) as device fp32 values read by the kernels.
+int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                            const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q,
                            const b2pa_tensor* cum_kv, int32_t max_q_len, int32_t max_kv_len, float bmm1_scale,
-                           float bmm2_scale, int32_t window_left, const b2pa_tensor* sinks, int32_t layout,
-                           b2pa_tensor* out, b2pa_stream_t stream_h)
+                           float bmm2_scale, const float* bmm1_dev, const float* bmm2_dev, int32_t window_left,
+                           const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, cudaStream_t stream)
 {
-    g_last_error.clear();
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     Problem pr;
     int st = parse_problem(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, sinks, layout, out, &pr);
     if (st)
@@ -539,7 +551,7 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         AttnParams ap;
         // a shape the tensor-core path accepts must encode; a failure is an
         // error of the call, never a silent switch to the other kernel
-        if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale)))
+        if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale, bmm1_dev, bmm2_dev)))
             return st;
         cudaError_t e = launch_schedule(sp, stream);
         if (e != cudaSuccess)
@@ -593,11 +605,51 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     gp.window = window;
     gp.scale_log2 = (float)((double)bmm1_scale * 1.4426950408889634);
     gp.bmm2 = bmm2_scale;
+    gp.bmm1_dev = bmm1_dev;
+    gp.bmm2_dev = bmm2_dev;
     gp.err = reinterpret_cast<unsigned*>(ws.mem);
     cudaError_t e = launch_attention_generic(gp, pr.fp8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "generic attention launch");
     return B2PA_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                           const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q,
+                           const b2pa_tensor* cum_kv, int32_t max_q_len, int32_t max_kv_len, float bmm1_scale,
+                           float bmm2_scale, int32_t window_left, const b2pa_tensor* sinks, int32_t layout,
+                           b2pa_tensor* out, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    return context_attention_impl(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, max_q_len, max_kv_len,
+                                  bmm1_scale, bmm2_scale, nullptr, nullptr, window_left, sinks, layout, out,
+                                  reinterpret_cast<cudaStream_t>(stream_h));
+}
+
+int b2pa_context_attention_tensor_scales(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                                         const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens,
+                                         const b2pa_tensor* cum_q, const b2pa_tensor* cum_kv, int32_t max_q_len,
+                                         int32_t max_kv_len, const b2pa_tensor* bmm1_scale,
+                                         const b2pa_tensor* bmm2_scale, int32_t window_left, const b2pa_tensor* sinks,
+                                         int32_t layout, b2pa_tensor* out, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    const float* b1 = scale_tensor(bmm1_scale, "bmm1_scale");
+    if (!b1)
+        return B2PA_ERR_INVALID_ARG;
+    const float* b2 = scale_tensor(bmm2_scale, "bmm2_scale");
+    if (!b2)
+        return B2PA_ERR_INVALID_ARG;
+    // the host values are placeholders that pass the host checks; the kernels use b1, b2
+    return context_attention_impl(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, max_q_len, max_kv_len,
+                                  1.0f, 1.0f, b1, b2, window_left, sinks, layout, out,
+                                  reinterpret_cast<cudaStream_t>(stream_h));
 }
 
 int b2pa_debug_worklist(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* block_tables,

@@ -69,6 +69,31 @@ __device__ __forceinline__ ItemGeom item_geometry(int q_len, int kv_len, int it,
     return g;
 }
 
+// The scales a kernel computes with: the host values, or the ones in device
+// memory when the call passed them as tensors (read once per thread;
+// bmm1_scale * log2(e) is formed in double and rounded once, as on the host).
+// ok = false when bmm1_scale is not finite and > 0 or bmm2_scale not finite.
+struct Scales {
+    float scale_log2;
+    float bmm2;
+    bool ok;
+};
+
+__device__ __forceinline__ Scales load_scales(float scale_log2, float bmm2, const float* bmm1_dev, const float* bmm2_dev)
+{
+    Scales sc{scale_log2, bmm2, true};
+    if (bmm1_dev != nullptr) {
+        const float b1 = *bmm1_dev;
+        sc.ok = isfinite(b1) && b1 > 0.f;
+        sc.scale_log2 = (float)((double)b1 * 1.4426950408889634);
+    }
+    if (bmm2_dev != nullptr) {
+        sc.bmm2 = *bmm2_dev;
+        sc.ok = sc.ok && isfinite(sc.bmm2);
+    }
+    return sc;
+}
+
 struct SchedParams {
     const int* cum_q;
     const int* seq_lens;
@@ -108,6 +133,8 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     int window;
     float scale_log2;    // bmm1_scale * log2(e)
     float bmm2;
+    const float* bmm1_dev;  // non-null: bmm1_scale is read from device memory (scale_log2 unused)
+    const float* bmm2_dev;  // non-null: bmm2_scale is read from device memory (bmm2 unused)
 };
 
 struct GatherParams {
@@ -142,6 +169,8 @@ struct GenericParams {
     int window;
     float scale_log2;
     float bmm2;
+    const float* bmm1_dev;  // as in AttnParams
+    const float* bmm2_dev;
     unsigned* err;
 };
 

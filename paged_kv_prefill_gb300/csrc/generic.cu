@@ -75,7 +75,13 @@ __global__ void __launch_bounds__(kGenericWarps * 32) generic_attention_kernel(c
     const int lo = p.window < 0 ? 0 : max(0, pos - p.window);
     const int G = p.H / p.Hkv;
     const int hk = h / G;
-    const float sl2 = p.scale_log2;
+    const Scales scl = load_scales(p.scale_log2, p.bmm2, p.bmm1_dev, p.bmm2_dev);
+    if (!scl.ok) {
+        if (lane == 0)
+            atomicOr(p.err, (unsigned)B2PA_DEV_BAD_SCALE);
+        return;
+    }
+    const float sl2 = scl.scale_log2;
 
     const uint16_t* qrow = p.q + (long long)tok * p.q_st_tok + (long long)h * p.q_st_head;
     for (int d = lane; d < p.D; d += 32)
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kGenericWarps * 32) generic_attention_kernel(c
     float total = l;
     if (p.sinks != nullptr && m != -INFINITY)
         total += exp2f(fmaf(p.sinks[h], kLog2e, -m));
-    const float inv = (m != -INFINITY && total > 0.f) ? p.bmm2 / total : 0.f;
+    const float inv = (m != -INFINITY && total > 0.f) ? scl.bmm2 / total : 0.f;
     uint16_t* orow = p.out + (long long)tok * p.out_st_tok + (long long)h * p.out_st_head;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {

@@ -112,6 +112,28 @@ def test_host_validation_without_gpu(lib):
     assert len(lib.b2pa_last_error_message()) > 0
 
 
+def test_tensor_scale_validation_without_gpu(lib):
+    """The device-tensor scales are checked on the host for what the host can
+    see: one fp32 element, 4-byte aligned, not null."""
+    BF, F32, I32 = 1, 3, 4
+    q = _fake([8, 4, 128], BF)
+    k = _fake([10, 2, 32, 128], BF)
+    bt, sl, cq = _fake([2, 4], I32), _fake([2], I32), _fake([3], I32)
+    r = ctypes.byref
+
+    def call(s1, s2):
+        return lib.b2pa_context_attention_tensor_scales(r(q), r(k), r(k), r(bt), r(sl), r(cq), None, 8, 8,
+                                                        None if s1 is None else r(s1), None if s2 is None else r(s2),
+                                                        -1, None, 0, r(q), None)
+
+    good = _fake([1], F32)
+    assert call(None, good) == -1
+    assert call(good, _fake([2], F32)) == -1                 # two elements
+    assert call(_fake([1], BF), good) == -1                  # not fp32
+    assert call(good, _fake([1], F32, base=(1 << 20) + 2)) == -1  # misaligned
+    assert b"bmm2_scale" in lib.b2pa_last_error_message()
+
+
 def test_binding_describes_torch_tensors():
     import paged_kv_prefill_gb300 as pkg
 
