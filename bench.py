@@ -302,7 +302,50 @@ def run_all_workloads(reps: int = 20):
                           "gflop": fl / 1e9, "algorithmic_mb": by / 1e6, "kernel_ms": k_ms, "call_ms": c_ms,
                           "kernel_tflops": fl / k_ms / 1e9, "call_tflops": fl / c_ms / 1e9,
                           "kernel_gbs": by / k_ms / 1e6, "device_status": b2pa.device_status()}), flush=True)
+    run_decode_workloads(reps)
     run_append_workloads(reps)
+
+
+def run_decode_workloads(reps: int = 20):
+    """One JSON line per decode batch (b2pa_batch_decode): median time of the
+    whole call (scheduler, attention over kv chunks, combine) after a 512 MiB L2
+    flush, with algorithmic GB/s against the copy peak; decode streams the KV
+    cache once, so HBM bandwidth is its roof."""
+    import paged_kv_prefill_gb300 as b2pa
+    from paged_kv_prefill_gb300 import build as b2pa_build
+
+    b2pa_build.build()
+    b2pa.load()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    _, hbm_gbs, _ = peaks()
+    for n, kvd in [(1, "bf16"), (4, "bf16"), (1, "fp8_e4m3")]:
+        inp = workload.decode_config(n, kv_dtype=kvd)
+        d = {k: getattr(inp, k).to(dev) for k in ("q", "k_pool", "v_pool", "block_tables", "seq_lens")}
+        out = torch.empty_like(d["q"])
+
+        def call():
+            b2pa.batch_decode(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], inp.max_kv_len,
+                              inp.bmm1_scale, inp.bmm2_scale, -1, out, inp.layout, None, q_len_per_req=n,
+                              stream=stream)
+
+        for _ in range(5):
+            call()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(reps)] for _ in range(2)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            flush.fill_(i)
+            ev[0][i].record(stream)
+            call()
+            ev[1][i].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in zip(ev[0], ev[1]))
+        by = algorithmic_bytes(inp)
+        print(json.dumps({"workload": inp.name, "q_len_per_req": n, "call_ms": ms, "algorithmic_mb": by / 1e6,
+                          "call_gbs": by / ms / 1e6, "frac_of_copy_peak": by / ms / 1e6 / hbm_gbs,
+                          "call_tflops": step_flops(inp) / ms / 1e9, "device_status": b2pa.device_status()}),
+              flush=True)
 
 
 def run_append_workloads(reps: int = 20):
@@ -631,6 +674,8 @@ def main():
                     help="time every named workload (kernel and call) and the K/V writes instead of the bench line")
     ap.add_argument("--append", action="store_true",
                     help="time only the K/V writes (b2pa_append_kv) of the bench and ragged FP8 workloads")
+    ap.add_argument("--decode", action="store_true",
+                    help="time only the decode batches (b2pa_batch_decode)")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K calls of the workload (for ncu); prints no measurement")
     args = ap.parse_args()
@@ -641,6 +686,9 @@ def main():
         return
     if args.append:
         run_append_workloads()
+        return
+    if args.decode:
+        run_decode_workloads()
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -150,6 +150,41 @@ B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_p
                            b2pa_stream_t stream);
 
 /*
+ * b2pa_batch_decode -- attention for a decode batch: every request has the
+ * same number of query tokens, q_len_per_req, the last ones of its sequence.
+ * This is the sibling call flashinfer.decode.trtllm_batch_decode_with_kv_cache
+ * that the TokenSpeed trtllm backend makes in forward_decode (query,
+ * kv_cache, block_tables, seq_lens, max_seq_len, bmm1_scale, bmm2_scale,
+ * window_left, sinks, q_len_per_req; q_len_per_req > 1 for speculative
+ * verification).  Query row i (0 <= i < q_len_per_req) of request b sits at
+ * position seq_lens[b] - q_len_per_req + i and sees keys as in
+ * b2pa_context_attention; the formula is the same.
+ *
+ * Arguments (device tensors) as for b2pa_context_attention, except:
+ *  q, out         [B * q_len_per_req, H, D] bf16: request b owns rows
+ *                 b * q_len_per_req .. (b + 1) * q_len_per_req - 1 (there is no
+ *                 cum_q and no cum_kv).
+ *  q_len_per_req  >= 1.
+ *  max_seq_len    upper bound on every seq_lens[b] (sizes the split below).
+ * A request with seq_lens[b] < q_len_per_req would have query rows with no
+ * visible key (the TokenSpeed backend clamps its seq_lens to avoid that,
+ * _clamped_spec_seqlens): it sets B2PA_DEV_BAD_REQUEST and its rows are not
+ * written.
+ *
+ * Few query rows per request cannot fill the GPU with one work item per
+ * request and kv head, so on the tensor-core path each request's kv range is
+ * cut into chunks (about two work items per SM over the batch's longest
+ * possible rows); the chunks' partial outputs go to the stream's workspace and
+ * a second kernel merges them.  Allocation, capture and error behaviour are
+ * those of b2pa_context_attention (the workspace also holds the partial rows:
+ * B * q_len_per_req * H * chunks * (D + 2) fp32).
+ */
+B2PA_API int b2pa_batch_decode(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                           const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, int32_t q_len_per_req,
+                           int32_t max_seq_len, float bmm1_scale, float bmm2_scale, int32_t window_left,
+                           const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, b2pa_stream_t stream);
+
+/*
  * b2pa_context_attention_tensor_scales -- b2pa_context_attention with
  * bmm1_scale and bmm2_scale given as device tensors instead of host floats.
  * The FlashInfer API reference types both as "float | Tensor": a serving

@@ -41,6 +41,7 @@ _DTYPES = {
 EXPORTED = [
     "b2pa_context_attention",
     "b2pa_context_attention_tensor_scales",
+    "b2pa_batch_decode",
     "b2pa_context_attention_noalloc",
     "b2pa_debug_worklist",
     "b2pa_debug_gather",
@@ -90,6 +91,9 @@ def load(path: str = LIB_PATH):
     lib.b2pa_context_attention_tensor_scales.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P,
                                                          ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
     lib.b2pa_context_attention_tensor_scales.restype = ctypes.c_int
+    lib.b2pa_batch_decode.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
+    lib.b2pa_batch_decode.restype = ctypes.c_int
     lib.b2pa_context_attention_noalloc.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, ctypes.c_int32, P,
                                                    ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_void_p]
@@ -215,6 +219,44 @@ def context_attention(
         int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
     )
     _check(st, "b2pa_context_attention")
+    return out
+
+
+def batch_decode(
+    query: torch.Tensor,
+    kv_cache: Union[torch.Tensor, Sequence[torch.Tensor]],
+    block_tables: torch.Tensor,
+    seq_lens: torch.Tensor,
+    max_seq_len: int,
+    bmm1_scale: float,
+    bmm2_scale: float,
+    window_left: int = -1,
+    out: Optional[torch.Tensor] = None,
+    kv_layout: str = "HND",
+    sinks: Optional[torch.Tensor] = None,
+    q_len_per_req: int = 1,
+    stream=None,
+) -> torch.Tensor:
+    """Decode attention over a paged KV cache: request b owns query rows
+    b * q_len_per_req .. + q_len_per_req - 1, the last q_len_per_req positions
+    of its seq_lens[b] keys (mirrors trtllm_batch_decode_with_kv_cache as the
+    TokenSpeed trtllm backend calls it; see include/b2pa.h)."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    if out is None:
+        out = torch.empty_like(query)
+    if isinstance(sinks, (list, tuple)):
+        if len(sinks) != 1:
+            raise ValueError("sinks: one fp32 [num_heads] tensor")
+        sinks = sinks[0]
+    dq, dk, dv, dbt, dsl = (desc(x) for x in (query, k, v, block_tables, seq_lens))
+    dsk, do = desc(sinks), desc(out)
+    st = lib.b2pa_batch_decode(
+        ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dbt), ctypes.byref(dsl),
+        int(q_len_per_req), int(max_seq_len), float(bmm1_scale), float(bmm2_scale), int(window_left), _ref(dsk),
+        LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
+    )
+    _check(st, "b2pa_batch_decode")
     return out
 
 

@@ -55,9 +55,11 @@
 
 namespace b2pa {
 
-constexpr int kItemRecWords = 10;  // a posted item: w, b, kvh, q0, q_len, kv_len, tok0, nq, n_lo, n_hi
+constexpr int kItemRecWords = 12;  // a posted item: w, b, kvh, q0, q_len, kv_len, tok0, nq, n_lo, n_hi, chunk, chunks
 
-template <int D, bool FP8>
+// SPLIT: the variant for split-KV work lists (decode batches), whose items are
+// kv chunks and whose split rows end in partial outputs
+template <int D, bool FP8, bool SPLIT>
 struct TcCfg {
     static constexpr int kHalves = D / 64;            // 128-byte column blocks per 16-bit row
     static constexpr int kHalfBytes = kQRows * 128;   // one column block of a 128-row tile
@@ -164,18 +166,30 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
 struct ItemInfo {
     int b, kvh, q0, q_len, kv_len;
     ItemGeom g;
+    int chunk, chunks;  // split-KV: this item's kv chunk and the request's chunk count (else 0, 1)
 };
 
+template <bool SPLIT>
 __device__ __forceinline__ ItemInfo read_item(const AttnParams& p, int w)
 {
     ItemInfo r;
     const int4 it = p.items[w];
     r.b = it.x;
     r.kvh = it.y;
-    r.q0 = p.cum_q[r.b];
-    r.q_len = p.cum_q[r.b + 1] - r.q0;
+    const QStarts cq{p.cum_q, p.q_per_req};
+    r.q0 = cq[r.b];
+    r.q_len = cq[r.b + 1] - r.q0;
     r.kv_len = p.seq_lens[r.b];
-    r.g = item_geometry(r.q_len, r.kv_len, it.z, p.rows_per_tile, p.window);
+    r.chunk = 0;
+    r.chunks = 1;
+    if (SPLIT) {
+        r.g = item_geometry(r.q_len, r.kv_len, 0, p.rows_per_tile, p.window);
+        r.chunk = it.z;
+        r.chunks = split_count(r.g, p.split_tiles);
+        split_range(&r.g, it.z, p.split_tiles);
+    } else {
+        r.g = item_geometry(r.q_len, r.kv_len, it.z, p.rows_per_tile, p.window);
+    }
     return r;
 }
 
@@ -200,6 +214,8 @@ __device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint
     it->g.nq = rec[7];
     it->g.n_lo = rec[8];
     it->g.n_hi = rec[9];
+    it->chunk = rec[10];
+    it->chunks = rec[11];
     __syncwarp();
     if ((threadIdx.x & 31) == 0)
         mbar_arrive(&c.bar.it_empty[s]);
@@ -210,10 +226,10 @@ __device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint
 // Producer: warp 0.  Lane 0 takes items; lane l loads page l of a kv tile (one
 // TMA box per 128-byte column block) after lane 0 posted the byte count.
 // ---------------------------------------------------------------------------
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void producer_role(const AttnParams& p, const Ctx& c)
 {
-    using C = TcCfg<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
     constexpr int kRingStages = FP8 ? C::kF8Stages : C::kStages;
     constexpr int kRingTileBytes = FP8 ? C::kF8TileBytes : C::kKvTileBytes;
     constexpr int kBoxes = FP8 ? 1 : C::kHalves;  // 128-byte-wide boxes per page
@@ -248,7 +264,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
                 w = -1;
             rec[0] = w;
             if (w >= 0) {
-                const ItemInfo r = read_item(p, w);
+                const ItemInfo r = read_item<SPLIT>(p, w);
                 rec[1] = r.b;
                 rec[2] = r.kvh;
                 rec[3] = r.q0;
@@ -258,6 +274,8 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
                 rec[7] = r.g.nq;
                 rec[8] = r.g.n_lo;
                 rec[9] = r.g.n_hi;
+                rec[10] = r.chunk;
+                rec[11] = r.chunks;
             }
             mbar_arrive(&c.bar.it_full[slot]);
         }
@@ -275,6 +293,8 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         it.g.nq = rec[7];
         it.g.n_lo = rec[8];
         it.g.n_hi = rec[9];
+        it.chunk = rec[10];
+        it.chunks = rec[11];
         // Q tiles, into the buffer of this item once its previous user is done
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
         if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c.abort_flag, p.err))
@@ -371,10 +391,10 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
 // MMA issuer: warp 1.  The whole warp waits and runs the issue code; the
 // MMAs and commits are predicated on lane 0, so the warp never diverges.
 // ---------------------------------------------------------------------------
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void mma_role(const AttnParams& p, const Ctx& c)
 {
-    using C = TcCfg<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
     // kind::f16; bf16 operands (f16 on the e4m3 path), f32 accumulators
     constexpr uint32_t kFmt = FP8 ? 0u : 1u;
     constexpr uint32_t kIdescS = (1u << 4) | (kFmt << 7) | (kFmt << 10) | ((uint32_t)(kKvTile >> 3) << 17) |
@@ -588,10 +608,10 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
 {
-    using C = TcCfg<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
     constexpr float kLog2e = 1.4426950408889634f;
     const int wq = (threadIdx.x >> 5) & 3;
     const int lane = threadIdx.x & 31;
@@ -788,7 +808,27 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         const float inv = (m_used != -INFINITY && total > 0.f) ? scl.bmm2 / total : 0.f;
         const float2 inv2 = make_float2(inv, inv);
         uint16_t* orow = p.out + (long long)(it.q0 + (valid ? i : 0)) * p.out_stride_tok + (long long)h * p.out_stride_head;
-        if constexpr (C::kStageOut) {
+        if (SPLIT && it.chunks > 1) {
+            // one kv chunk of a split row: the unnormalised O and (m, l) in the
+            // running maximum's log2 units; the combine kernel merges the chunks,
+            // adds the sink term and applies bmm2_scale / denominator
+            const long long slot = ((long long)(it.q0 + (valid ? i : 0)) * p.H + h) * p.part_slots + it.chunk;
+            float4* po = reinterpret_cast<float4*>(p.part_o + slot * D);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(o_tmem + (uint32_t)(q * 32), o);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        po[q * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                                    __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+                }
+            }
+            if (valid)
+                *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(m_used, l);
+        } else if constexpr (C::kStageOut) {
             // each 64-column half of the warp's 32 rows goes through shared
             // memory (row r in 128 bytes, 16-byte chunks swizzled by r % 8: the
             // 128-byte swizzle of the output tensor map).  When all 32 rows are
@@ -897,10 +937,10 @@ __device__ __forceinline__ int q_row_exponent(uint32_t mx)
 }
 
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void convert_role(const AttnParams& p, const Ctx& c)
 {
-    using C = TcCfg<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
     const int ct = threadIdx.x - 12 * 32;  // 0..127: tile row
     const int lane = threadIdx.x & 31;
     const int sw = ct & 7;                 // 128-byte swizzle phase of this row
@@ -998,10 +1038,10 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool FP8>
-__global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kernel(const __grid_constant__ AttnParams p)
+template <int D, bool FP8, bool SPLIT>
+__global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_tc_kernel(const __grid_constant__ AttnParams p)
 {
-    using C = TcCfg<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -1098,27 +1138,27 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
         if (warp < 4) {
             regs_dec<88>();
             if (warp == 0)
-                producer_role<D, FP8>(p, c);
+                producer_role<D, FP8, SPLIT>(p, c);
             else if (warp == 1)
-                mma_role<D, FP8>(p, c);
+                mma_role<D, FP8, SPLIT>(p, c);
         } else if (warp < 12) {
             regs_inc<176>();
-            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+            softmax_role<D, FP8, SPLIT>(p, c, (warp - 4) >> 2);
         } else {
             regs_dec<72>();
-            convert_role<D, FP8>(p, c);
+            convert_role<D, FP8, SPLIT>(p, c);
         }
     } else {
         // 384 threads launch with 168 registers each (104 + 200 + 200 = 504 = 3 x 168)
         if (warp < 4) {
             regs_dec<104>();
             if (warp == 0)
-                producer_role<D, FP8>(p, c);
+                producer_role<D, FP8, SPLIT>(p, c);
             else if (warp == 1)
-                mma_role<D, FP8>(p, c);
+                mma_role<D, FP8, SPLIT>(p, c);
         } else {
             regs_inc<200>();
-            softmax_role<D, FP8>(p, c, (warp - 4) >> 2);
+            softmax_role<D, FP8, SPLIT>(p, c, (warp - 4) >> 2);
         }
     }
 
@@ -1130,11 +1170,11 @@ __global__ void __launch_bounds__(TcCfg<D, FP8>::kThreads, 1) attention_tc_kerne
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 static cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream, bool pdl)
 {
-    using C = TcCfg<D, FP8>;
-    auto kern = attention_tc_kernel<D, FP8>;
+    using C = TcCfg<D, FP8, SPLIT>;
+    auto kern = attention_tc_kernel<D, FP8, SPLIT>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -1162,15 +1202,22 @@ static cudaError_t launch_one(const AttnParams& p, int grid, cudaStream_t stream
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl)
+template <bool SPLIT>
+static cudaError_t launch_variant(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl)
 {
     if (fp8)
-        return head_dim == 128 ? launch_one<128, true>(p, grid, stream, pdl) : cudaErrorInvalidValue;
+        return head_dim == 128 ? launch_one<128, true, SPLIT>(p, grid, stream, pdl) : cudaErrorInvalidValue;
     if (head_dim == 128)
-        return launch_one<128, false>(p, grid, stream, pdl);
+        return launch_one<128, false, SPLIT>(p, grid, stream, pdl);
     if (head_dim == 64)
-        return launch_one<64, false>(p, grid, stream, pdl);
+        return launch_one<64, false, SPLIT>(p, grid, stream, pdl);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl)
+{
+    return p.split_tiles > 0 ? launch_variant<true>(p, head_dim, fp8, grid, stream, pdl)
+                             : launch_variant<false>(p, head_dim, fp8, grid, stream, pdl);
 }
 
 }  // namespace b2pa

@@ -89,9 +89,15 @@ std::mutex g_ws_mu;
 std::vector<Workspace> g_ws;
 constexpr size_t kWsHeader = 256;
 
+int get_workspace_bytes(int dev, cudaStream_t stream, size_t need, Workspace* out);
+
 int get_workspace(int dev, cudaStream_t stream, size_t items, Workspace* out)
 {
-    const size_t need = kWsHeader + items * sizeof(int4);
+    return get_workspace_bytes(dev, stream, kWsHeader + items * sizeof(int4), out);
+}
+
+int get_workspace_bytes(int dev, cudaStream_t stream, size_t need, Workspace* out)
+{
     std::lock_guard<std::mutex> lk(g_ws_mu);
     for (auto& w : g_ws) {
         if (w.dev == dev && w.stream == stream) {
@@ -188,6 +194,7 @@ struct Problem {
     long long k_st[3], v_st[3];  // page, head, slot (elements)
     const void *q, *k, *v;
     const int *bt, *seq, *cum_q, *cum_kv;
+    int q_per_req;  // > 0: decode batch, request b owns query rows b * q_per_req .. (cum_q null)
     const float* sinks;
     void* out;
 };
@@ -230,7 +237,7 @@ int parse_pools(const b2pa_tensor* k, const b2pa_tensor* v, int32_t layout, Prob
 int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                   const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q,
                   const b2pa_tensor* cum_kv, const b2pa_tensor* sinks, int32_t layout, const b2pa_tensor* out,
-                  Problem* pr)
+                  Problem* pr, int32_t q_per_req = 0)
 {
     std::memset(pr, 0, sizeof *pr);
     int st = parse_pools(k_pool, v_pool, layout, pr);
@@ -267,8 +274,13 @@ int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_te
     pr->B = (int)B;
     if (B > 0 && !is_vec(seq_lens, B2PA_INT32, B))
         return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
-    if (!is_vec(cum_q, B2PA_INT32, B + 1))
+    if (q_per_req > 0) {
+        if ((long long)B * q_per_req != (long long)pr->T)
+            return fail(B2PA_ERR_INVALID_ARG, "q must hold batch x q_len_per_req = %lld x %d tokens, not %d",
+                        (long long)B, q_per_req, pr->T);
+    } else if (!is_vec(cum_q, B2PA_INT32, B + 1)) {
         return fail(B2PA_ERR_INVALID_ARG, "cum_q must be contiguous int32 [B + 1]");
+    }
     if (cum_kv && !is_vec(cum_kv, B2PA_INT32, B + 1))
         return fail(B2PA_ERR_INVALID_ARG, "cum_kv must be contiguous int32 [B + 1] (or NULL)");
     if (!block_tables || block_tables->ndim != 2 || block_tables->dtype != B2PA_INT32 ||
@@ -281,7 +293,8 @@ int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_te
     pr->bt_stride = block_tables->stride[0];
     pr->bt = static_cast<const int*>(block_tables->data);
     pr->seq = static_cast<const int*>(B > 0 ? seq_lens->data : nullptr);
-    pr->cum_q = static_cast<const int*>(cum_q->data);
+    pr->cum_q = q_per_req > 0 ? nullptr : static_cast<const int*>(cum_q->data);
+    pr->q_per_req = q_per_req > 0 ? q_per_req : 0;
     pr->cum_kv = cum_kv ? static_cast<const int*>(cum_kv->data) : nullptr;
     if (sinks) {
         if (!is_vec(sinks, B2PA_FP32, pr->H))
@@ -421,6 +434,7 @@ int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, s
     encode_o_map(&ap->tm_o, pr, &o_ok);
     ap->out_tma = o_ok ? 1 : 0;
     ap->cum_q = pr.cum_q;
+    ap->q_per_req = pr.q_per_req;
     ap->seq_lens = pr.seq;
     ap->block_tables = pr.bt;
     ap->sinks = pr.sinks;
@@ -489,6 +503,7 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     SchedParams sp;
     std::memset(&sp, 0, sizeof sp);
     sp.cum_q = pr.cum_q;
+    sp.q_per_req = pr.q_per_req;
     sp.seq_lens = pr.seq;
     sp.cum_kv = pr.cum_kv;
     sp.block_tables = pr.bt;
@@ -516,16 +531,49 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     return sp;
 }
 
-// Both attention entry points: scales as host floats, or (bmm1_dev, bmm2_dev
+// Split-KV geometry of a decode batch on the tensor-core path: chunks of
+// split_tiles kv tiles, at most `slots` chunks per request (split_tiles = 0:
+// no split).  The chunk size gives the batch about two work items per SM on
+// its longest possible rows (the lengths themselves are on the device), and
+// never fewer than two kv tiles per chunk.
+struct SplitPlan {
+    int split_tiles = 0;
+    int slots = 1;
+};
+
+SplitPlan plan_split(const Problem& pr, int max_kv_len, int sms)
+{
+    SplitPlan sp;
+    const int G = pr.H / pr.Hkv;
+    const int per_item = (kQRows / G) * kQTiles;
+    if (pr.q_per_req <= 0 || pr.q_per_req > per_item)
+        return sp;  // several query items per request: no split (as a context batch)
+    const long long tiles = (max_kv_len + kKvTile - 1) / kKvTile;
+    const long long total = (long long)pr.B * pr.Hkv * tiles;
+    const long long want = 2LL * sms;
+    long long chunk = (total + want - 1) / want;
+    if (chunk < 2)
+        chunk = 2;
+    if (chunk >= tiles)
+        return sp;  // enough items without cutting any request
+    sp.split_tiles = (int)chunk;
+    sp.slots = (int)((tiles + chunk - 1) / chunk);
+    return sp;
+}
+
+// Every attention entry point: a context batch (cum_q) or a decode batch
+// (q_per_req > 0, cum_q null); scales as host floats, or (bmm1_dev, bmm2_dev
 // non-null) as device fp32 values read by the kernels.
 int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                            const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q,
                            const b2pa_tensor* cum_kv, int32_t max_q_len, int32_t max_kv_len, float bmm1_scale,
                            float bmm2_scale, const float* bmm1_dev, const float* bmm2_dev, int32_t window_left,
-                           const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, cudaStream_t stream)
+                           const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, cudaStream_t stream,
+                           int32_t q_per_req = 0)
 {
     Problem pr;
-    int st = parse_problem(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, sinks, layout, out, &pr);
+    int st = parse_problem(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, sinks, layout, out, &pr,
+                           q_per_req);
     if (st)
         return st;
     if (max_q_len < 0 || max_kv_len < 0)
@@ -543,9 +591,16 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     if ((st = choose_path(pr, di, &use_tc)))
         return st;
     if (use_tc) {
-        const size_t cap = items_needed(pr, max_q_len);
+        const SplitPlan split = plan_split(pr, max_kv_len, di.sms);
+        const size_t cap = split.split_tiles > 0 ? (size_t)pr.B * pr.Hkv * split.slots : items_needed(pr, max_q_len);
+        // workspace: header, work list, then (split-KV) chunks per request and the partial rows
+        const size_t rows = (size_t)pr.T * pr.H * split.slots;
+        const size_t off_nsplit = kWsHeader + cap * sizeof(int4);
+        const size_t off_ml = (off_nsplit + (size_t)pr.B * sizeof(int) + 255) / 256 * 256;
+        const size_t off_o = (off_ml + rows * 2 * sizeof(float) + 255) / 256 * 256;
+        const size_t need = split.split_tiles > 0 ? off_o + rows * pr.D * sizeof(float) : off_nsplit;
         Workspace ws;
-        if ((st = get_workspace(dev, stream, cap, &ws)))
+        if ((st = get_workspace_bytes(dev, stream, need, &ws)))
             return st;
         SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
         AttnParams ap;
@@ -553,6 +608,17 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         // error of the call, never a silent switch to the other kernel
         if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale, bmm1_dev, bmm2_dev)))
             return st;
+        if (split.split_tiles > 0) {
+            sp.split_tiles = split.split_tiles;
+            sp.nsplit = reinterpret_cast<int*>(ws.mem + off_nsplit);
+            // chunk costs are at most split_tiles * kQTiles
+            const int nb = split.split_tiles * kQTiles + 1;
+            sp.nbuckets = nb < sp.nbuckets ? nb : sp.nbuckets;
+            ap.split_tiles = split.split_tiles;
+            ap.part_slots = split.slots;
+            ap.part_ml = reinterpret_cast<float*>(ws.mem + off_ml);
+            ap.part_o = reinterpret_cast<float*>(ws.mem + off_o);
+        }
         cudaError_t e = launch_schedule(sp, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "scheduler launch");
@@ -566,6 +632,26 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
             return cuda_fail(e, "attention kernel launch");
         if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
+        if (split.split_tiles > 0) {
+            CombineParams cp;
+            std::memset(&cp, 0, sizeof cp);
+            cp.part_o = ap.part_o;
+            cp.part_ml = ap.part_ml;
+            cp.nsplit = sp.nsplit;
+            cp.sinks = pr.sinks;
+            cp.out = static_cast<uint16_t*>(pr.out);
+            cp.out_st_tok = pr.out_st_tok;
+            cp.out_st_head = pr.out_st_head;
+            cp.B = pr.B;
+            cp.q_per_req = pr.q_per_req;
+            cp.H = pr.H;
+            cp.D = pr.D;
+            cp.part_slots = split.slots;
+            cp.bmm2 = bmm2_scale;
+            cp.bmm2_dev = bmm2_dev;
+            if ((e = launch_combine(cp, stream)) != cudaSuccess)
+                return cuda_fail(e, "combine launch");
+        }
         return B2PA_OK;
     }
     Workspace ws;
@@ -577,6 +663,7 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     gp.k = pr.k;
     gp.v = pr.v;
     gp.cum_q = pr.cum_q;
+    gp.q_per_req = pr.q_per_req;
     gp.seq_lens = pr.seq;
     gp.block_tables = pr.bt;
     gp.sinks = pr.sinks;
@@ -630,6 +717,19 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     return context_attention_impl(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, max_q_len, max_kv_len,
                                   bmm1_scale, bmm2_scale, nullptr, nullptr, window_left, sinks, layout, out,
                                   reinterpret_cast<cudaStream_t>(stream_h));
+}
+
+int b2pa_batch_decode(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                      const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, int32_t q_len_per_req,
+                      int32_t max_seq_len, float bmm1_scale, float bmm2_scale, int32_t window_left,
+                      const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    if (q_len_per_req < 1)
+        return fail(B2PA_ERR_INVALID_ARG, "q_len_per_req must be >= 1");
+    return context_attention_impl(q, k_pool, v_pool, block_tables, seq_lens, nullptr, nullptr, q_len_per_req,
+                                  max_seq_len, bmm1_scale, bmm2_scale, nullptr, nullptr, window_left, sinks, layout,
+                                  out, reinterpret_cast<cudaStream_t>(stream_h), q_len_per_req);
 }
 
 int b2pa_context_attention_tensor_scales(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,

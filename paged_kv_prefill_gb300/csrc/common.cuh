@@ -19,6 +19,14 @@ constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 5 words per request in shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait that exceeds this gives up
 
+// Where request b's query rows start: cum_q[b], or b * q_per_req for a decode
+// batch, whose requests all have q_per_req query tokens (cum_q null).
+struct QStarts {
+    const int* cum_q;
+    int q_per_req;
+    __device__ __forceinline__ int operator[](int b) const { return cum_q != nullptr ? cum_q[b] : b * q_per_req; }
+};
+
 // A request is processed only if its lengths are consistent with the bounds
 // the caller gave; otherwise the scheduler sets B2PA_DEV_BAD_REQUEST.
 struct RequestView {
@@ -28,7 +36,7 @@ struct RequestView {
     bool ok;
 };
 
-__device__ __forceinline__ RequestView load_request(const int* cum_q, const int* seq_lens, int b, int max_q_len,
+__device__ __forceinline__ RequestView load_request(QStarts cum_q, const int* seq_lens, int b, int max_q_len,
                                                     int max_kv_len, int page_size, int max_pages, int num_tokens)
 {
     RequestView r;
@@ -69,6 +77,19 @@ __device__ __forceinline__ ItemGeom item_geometry(int q_len, int kv_len, int it,
     return g;
 }
 
+// Split-KV (decode batches): a request's single work item per kv head is cut
+// into chunks of `split_tiles` kv tiles; chunk s covers tiles
+// n_lo + s * split_tiles .. (clipped to n_hi).
+__device__ __forceinline__ int split_count(const ItemGeom& g, int split_tiles)
+{
+    return (g.n_hi - g.n_lo + split_tiles) / split_tiles;
+}
+__device__ __forceinline__ void split_range(ItemGeom* g, int s, int split_tiles)
+{
+    g->n_lo += s * split_tiles;
+    g->n_hi = min(g->n_hi, g->n_lo + split_tiles - 1);
+}
+
 // The scales a kernel computes with: the host values, or the ones in device
 // memory when the call passed them as tensors (read once per thread;
 // bmm1_scale * log2(e) is formed in double and rounded once, as on the host).
@@ -95,7 +116,8 @@ __device__ __forceinline__ Scales load_scales(float scale_log2, float bmm2, cons
 }
 
 struct SchedParams {
-    const int* cum_q;
+    const int* cum_q;         // null: q_per_req query tokens per request (decode batch)
+    int q_per_req;
     const int* seq_lens;
     const int* cum_kv;        // may be null
     const int* block_tables;  // read only when debug != 0
@@ -104,6 +126,8 @@ struct SchedParams {
     int debug;
     int cap;
     int nbuckets;             // cost buckets in use: min(kSchedBuckets, largest possible cost + 1)
+    int split_tiles;          // > 0: split-KV items (one query item per request and kv head, cut in chunks)
+    int* nsplit;              // split-KV: chunks per request (0 for a request without work), for the combine
     int4* items;
     int* count;
     int* counter;             // work counter of the attention kernel, reset here
@@ -116,11 +140,16 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     CUtensorMap tm_v;
     CUtensorMap tm_o;   // 3-D: (D, H, T), box (64, min(G, 32), max(1, 32 / G)): one warp's 32 rows
     int out_tma;        // 1: tm_o is valid and a warp's 32 rows are whole boxes (G divides 32 or 32 divides G)
-    const int* cum_q;
+    const int* cum_q;    // null: q_per_req query tokens per request
+    int q_per_req;
     const int* seq_lens;
     const int* block_tables;
     const float* sinks;  // may be null
     uint16_t* out;       // bf16 bits
+    int split_tiles;     // > 0: items are kv chunks; a chunk of a request cut in several writes partials
+    int part_slots;      // chunks per row in the partial buffers
+    float* part_o;       // [(token * H + head) * part_slots + chunk][D] unnormalised O (f32)
+    float* part_ml;      // [(token * H + head) * part_slots + chunk][2] running maximum (log2 units) and sum
     long long bt_stride;
     long long out_stride_tok;
     long long out_stride_head;
@@ -155,7 +184,8 @@ struct GenericParams {
     const uint16_t* q;
     const void* k;
     const void* v;
-    const int* cum_q;
+    const int* cum_q;    // null: q_per_req query tokens per request
+    int q_per_req;
     const int* seq_lens;
     const int* block_tables;
     const float* sinks;
@@ -174,10 +204,24 @@ struct GenericParams {
     unsigned* err;
 };
 
+// Merging the chunks of split-KV rows (decode batches): one warp per output row.
+struct CombineParams {
+    const float* part_o;
+    const float* part_ml;
+    const int* nsplit;   // chunks per request (<= 1: the attention kernel wrote the row)
+    const float* sinks;  // may be null
+    uint16_t* out;
+    long long out_st_tok, out_st_head;
+    int B, q_per_req, H, D, part_slots;
+    float bmm2;
+    const float* bmm2_dev;
+};
+
 // Host launchers (one translation unit each).
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaStream_t stream);
 cudaError_t launch_attention_generic(const GenericParams& p, bool fp8, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 }  // namespace b2pa

@@ -46,7 +46,9 @@ __global__ void __launch_bounds__(kGenericWarps * 32) generic_attention_kernel(c
     float* qs = qs_all + warp * p.D;
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b < p.B; b += blockDim.x)
-            if (!load_request(p.cum_q, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size, p.max_pages, p.T).ok)
+            if (!load_request(QStarts{p.cum_q, p.q_per_req}, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size,
+                              p.max_pages, p.T)
+                     .ok)
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
     }
     const long long rowid = (long long)blockIdx.x * kGenericWarps + warp;
@@ -55,17 +57,20 @@ __global__ void __launch_bounds__(kGenericWarps * 32) generic_attention_kernel(c
     const int tok = (int)(rowid / p.H), h = (int)(rowid % p.H);
 
     // the request owning this token: last b with cum_q[b] <= tok
+    const QStarts cq{p.cum_q, p.q_per_req};
     int lo_b = 0, hi_b = p.B - 1;
+    if (p.cum_q == nullptr) {
+        lo_b = hi_b = min(p.B - 1, tok / p.q_per_req);
+    }
     while (lo_b < hi_b) {
         const int mid = (lo_b + hi_b + 1) >> 1;
-        if (p.cum_q[mid] <= tok)
+        if (cq[mid] <= tok)
             lo_b = mid;
         else
             hi_b = mid - 1;
     }
     const int b = lo_b;
-    const RequestView r =
-        load_request(p.cum_q, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size, p.max_pages, p.T);
+    const RequestView r = load_request(cq, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size, p.max_pages, p.T);
     if (!r.ok)
         return;
     if (tok < r.q_start || tok >= r.q_start + r.q_len)

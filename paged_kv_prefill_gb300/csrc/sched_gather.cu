@@ -11,7 +11,9 @@ namespace b2pa {
 // Scheduler: one CTA of 1024 threads.
 //
 // 1. Validate each request (load_request) and count its items:
-//    Hkv * ceil(q_len / (rows_per_tile * kQTiles)).
+//    Hkv * ceil(q_len / (rows_per_tile * kQTiles)), times the number of kv
+//    chunks for split-KV (decode) batches, whose one item per kv head is cut
+//    in chunks of split_tiles kv tiles (item.z = chunk index there).
 // 2. Enumerate items in (b, kv head, it) order; cost = kv tiles x non-empty
 //    query tiles (item_geometry), bucket = min(cost, kCostCap).
 // 3. Stable counting sort by bucket, descending (p.nbuckets buckets: as many as
@@ -82,15 +84,23 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
     const int b_begin = min(B, tid * chunk), b_end = min(B, b_begin + chunk);
     int local = 0;
     for (int b = b_begin; b < b_end; ++b) {
-        const RequestView r = load_request(p.cum_q, p.seq_lens, b, p.max_q_len, p.max_kv_len, p.page_size,
-                                           p.max_pages, p.num_tokens);
+        const RequestView r = load_request(QStarts{p.cum_q, p.q_per_req}, p.seq_lens, b, p.max_q_len, p.max_kv_len,
+                                           p.page_size, p.max_pages, p.num_tokens);
         if (!r.ok)
             atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
-        const int n = (r.ok && r.q_len > 0) ? p.Hkv * ((r.q_len + per_item - 1) / per_item) : 0;
+        int n_it = (r.ok && r.q_len > 0) ? (r.q_len + per_item - 1) / per_item : 0;  // items per kv head
+        if (p.split_tiles > 0) {
+            // one query item per kv head (the host makes q_len fit), cut in kv chunks
+            const int ns = n_it > 0 ? split_count(item_geometry(r.q_len, r.kv_len, 0, p.rows_per_tile, p.window),
+                                                  p.split_tiles)
+                                    : 0;
+            p.nsplit[b] = ns;
+            n_it = ns;
+        }
+        const int n = p.Hkv * n_it;
         req_start[b] = n;  // count for now
         req_q[b] = r.q_len;
         req_kv[b] = r.kv_len;
-        const int n_it = (r.q_len + per_item - 1) / per_item;
         req_nit[b] = n_it;
         req_inv[b] = n_it > 0 ? 1.0f / (float)n_it : 0.f;
         local += n;
@@ -144,8 +154,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
             --kvh;
         while ((kvh + 1) * n_it <= loc)
             ++kvh;
-        const int it = loc - kvh * n_it;
-        const ItemGeom g = item_geometry(q_len, kv_len, it, p.rows_per_tile, p.window);
+        const int it = loc - kvh * n_it;  // split-KV: the chunk index (the query item is 0)
+        ItemGeom g = item_geometry(q_len, kv_len, p.split_tiles > 0 ? 0 : it, p.rows_per_tile, p.window);
+        if (p.split_tiles > 0)
+            split_range(&g, it, p.split_tiles);
         const int cost = (g.n_hi - g.n_lo + 1) * g.nq;
         item = make_int4(b, kvh, it, cost);
         bucket = min(cost, nb - 1);

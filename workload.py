@@ -306,3 +306,20 @@ def config(index: int, window_left: Optional[int] = None, seed: Optional[int] = 
         return build(ql, kv, 32, 8, 128, 32, "HND", kv_dtype="fp8_e4m3", pool_factor=2.0,
                      seed=s, name=name, q_scale=q_scale)
     raise ValueError(index)
+
+
+# ---------------------------------------------------------------------------
+# Decode batches (the decode sibling): every request holds q_len_per_req query
+# tokens, the last of its kv sequence (TokenSpeed trtllm backend,
+# forward_decode; q_len_per_req > 1 is speculative verification).  Shaped like
+# the ragged FP8 workload's long rows: 32 requests, kv lengths uniform in
+# [q_len_per_req, 32768], H 32 / Hkv 8, D 128, P 32, HND, bf16.
+# ---------------------------------------------------------------------------
+
+def decode_config(q_len_per_req: int = 1, seed: Optional[int] = None, kv_dtype: str = "bf16") -> Inputs:
+    s = 1300 + q_len_per_req if seed is None else seed
+    g = torch.Generator().manual_seed(s)
+    kv = _uniform_int(g, q_len_per_req, 32768, 32)
+    name = f"decode_b32_q{q_len_per_req}_kv-32768_h32kv8_d128_p32_hnd" + ("" if kv_dtype == "bf16" else "_fp8kv")
+    return build([q_len_per_req] * 32, kv, 32, 8, 128, 32, "HND", kv_dtype=kv_dtype, pool_factor=2.0, seed=s,
+                 name=name)
