@@ -150,6 +150,37 @@ B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_p
                            b2pa_stream_t stream);
 
 /*
+ * b2pa_context_attention_ragged -- b2pa_context_attention with the ragged
+ * page table instead of a [B, max_pages] block table: FlashInfer's
+ * paged_kv_indices / paged_kv_indptr / paged_kv_last_page_len (TensorRT-LLM
+ * teardown (6), "Attention Backend 的 prepare() 内部", section "三条路径之二:
+ * FlashInferAttentionMetadata——page table 三件套").  The page ids of all
+ * requests are concatenated into one flat array, so a batch of short and long
+ * requests carries no padding columns.
+ *
+ *  paged_kv_indices        int32 [nnz], contiguous: the page ids of request b
+ *                          are paged_kv_indices[indptr[b] .. indptr[b+1]), in
+ *                          logical order (key j on page j / P, slot j % P).
+ *  paged_kv_indptr         int32 [B + 1], contiguous, non-decreasing from
+ *                          indptr[0] (normally 0); B = its length - 1.
+ *  paged_kv_last_page_len  int32 [B], contiguous: valid tokens of request b's
+ *                          last page, in [1, P] when it has pages.
+ * Request b's kv length is (indptr[b+1] - indptr[b] - 1) * P +
+ * last_page_len[b] (0 without pages); it replaces seq_lens, and cum_kv is not
+ * taken.  A request with a decreasing indptr or a last_page_len outside
+ * [1, P] sets B2PA_DEV_BAD_REQUEST and its rows are not written.  The kv
+ * lengths are derived on the device into the stream's workspace (B int32).
+ * Every other argument, the layout rules and the errors are those of
+ * b2pa_context_attention.
+ */
+B2PA_API int b2pa_context_attention_ragged(const b2pa_tensor* q, const b2pa_tensor* k_pool,
+                           const b2pa_tensor* v_pool, const b2pa_tensor* paged_kv_indices,
+                           const b2pa_tensor* paged_kv_indptr, const b2pa_tensor* paged_kv_last_page_len,
+                           const b2pa_tensor* cum_q, int32_t max_q_len, int32_t max_kv_len, float bmm1_scale,
+                           float bmm2_scale, int32_t window_left, const b2pa_tensor* sinks, int32_t layout,
+                           b2pa_tensor* out, b2pa_stream_t stream);
+
+/*
  * b2pa_batch_decode -- attention for a decode batch: every request has the
  * same number of query tokens, q_len_per_req, the last ones of its sequence.
  * This is the sibling call flashinfer.decode.trtllm_batch_decode_with_kv_cache
@@ -285,6 +316,17 @@ B2PA_API int b2pa_debug_worklist(const b2pa_tensor* q, const b2pa_tensor* k_pool
  */
 B2PA_API int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
                       const b2pa_tensor* seq_lens, const b2pa_tensor* cum_kv, int32_t layout,
+                      b2pa_tensor* k_out, b2pa_tensor* v_out, b2pa_stream_t stream);
+
+/*
+ * b2pa_debug_gather_ragged -- b2pa_debug_gather for the ragged page table
+ * (see b2pa_context_attention_ragged): the first kv_len(b) tokens of every
+ * request, their pages found through the same shared addressing as the
+ * attention kernel's loads, to k_out / v_out at row offset cum_kv[b].
+ */
+B2PA_API int b2pa_debug_gather_ragged(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                      const b2pa_tensor* paged_kv_indices, const b2pa_tensor* paged_kv_indptr,
+                      const b2pa_tensor* paged_kv_last_page_len, const b2pa_tensor* cum_kv, int32_t layout,
                       b2pa_tensor* k_out, b2pa_tensor* v_out, b2pa_stream_t stream);
 
 /*

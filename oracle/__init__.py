@@ -66,6 +66,8 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_append_kv.restype = ctypes.c_int64
+        lib.oracle_gather_ragged.restype = ctypes.c_int
+        lib.oracle_ragged_lengths.restype = None
         _lib = lib
     return _lib
 
@@ -204,3 +206,55 @@ def worklist(inp, rows_per_tile: int, n_qtiles: int, kv_tile: int, cost_cap: int
     if n < 0:
         raise ValueError("work list larger than cap")
     return out[:n].copy()
+
+
+def ragged_lengths(indptr: torch.Tensor, last_page_len: torch.Tensor, page_size: int) -> torch.Tensor:
+    """Kv length of each request of a ragged page table (-1: malformed)."""
+    lib = _load()
+    ip = indptr.to(torch.int32).contiguous()
+    lp = last_page_len.to(torch.int32).contiguous()
+    B = ip.numel() - 1
+    out = torch.zeros((max(B, 0),), dtype=torch.int32)
+    lib.oracle_ragged_lengths(_ptr(ip), _ptr(lp), ctypes.c_int(B), ctypes.c_int(page_size), _ptr(out))
+    return out
+
+
+def gather_ragged(inp, indices, indptr, last_page_len, which: str = "k"):
+    """Contiguous [sum(kv lengths), Hkv, D] copy of the K (or V) tokens through a
+    ragged page table, at row offsets inp.cum_kv.  Returns (tensor, ok)."""
+    lib = _load()
+    pool = inp.k_pool if which == "k" else inp.v_pool
+    kv = ragged_lengths(indptr, last_page_len, inp.page_size)
+    ends = inp.cum_kv[:-1].to(torch.int64) + kv.clamp_min(0).to(torch.int64)
+    total = max(int(inp.cum_kv[-1]), int(ends.max()) if ends.numel() else 0)  # every row the gather may write
+    out = torch.zeros((total, inp.num_kv_heads, inp.head_dim), dtype=pool.dtype)
+    p = _pool(pool)
+    idx = indices.to(torch.int32).contiguous()
+    ip = indptr.to(torch.int32).contiguous()
+    lp = last_page_len.to(torch.int32).contiguous()
+    rc = lib.oracle_gather_ragged(ctypes.byref(p), ctypes.c_int(LAYOUTS[inp.layout]), _ptr(idx), _ptr(ip), _ptr(lp),
+                                  _ptr(inp.cum_kv.contiguous()), ctypes.c_int(ip.numel() - 1),
+                                  ctypes.c_void_p(out.data_ptr()))
+    return out, rc == 0
+
+
+def attention_ragged(inp, indices, indptr, last_page_len, rows=None, threads: int | None = None):
+    """attention() for a batch whose pages come from a ragged page table: each
+    request's slice of the flat page ids becomes its block-table row and its kv
+    length follows the ragged rule; inp supplies q, the pools, cum_q, scales,
+    window and sinks."""
+    import copy
+
+    kv = ragged_lengths(indptr, last_page_len, inp.page_size)
+    B = kv.numel()
+    ip = indptr.tolist()
+    width = max([ip[b + 1] - ip[b] for b in range(B)] + [1])
+    table = torch.full((B, width), -1, dtype=torch.int32)
+    for b in range(B):
+        n = ip[b + 1] - ip[b]
+        if n > 0:
+            table[b, :n] = indices[ip[b]:ip[b + 1]].to(torch.int32)
+    r = copy.copy(inp)
+    r.block_tables = table
+    r.seq_lens = kv
+    return attention(r, rows=rows, threads=threads)

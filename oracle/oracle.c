@@ -166,6 +166,74 @@ int oracle_gather(const oracle_pool* pool, int layout, const int32_t* block_tabl
 }
 
 /*
+ * The ragged page table (FlashInfer's paged_kv_indices / paged_kv_indptr /
+ * paged_kv_last_page_len; TensorRT-LLM teardown (6), section "三条路径之二:
+ * FlashInferAttentionMetadata——page table 三件套"): the page ids of every
+ * request concatenated into one flat array, indptr[b] .. indptr[b + 1] the
+ * slice of request b, and last_page_len[b] the valid tokens in its last page.
+ *
+ * Kv length of request b: its pages hold P tokens each except the last, which
+ * holds last_page_len[b]: (pages - 1) * P + last_page_len[b], or 0 without
+ * pages.  A negative page count, or a last_page_len outside [1, P] with pages,
+ * is malformed: length -1.
+ */
+void oracle_ragged_lengths(const int32_t* indptr, const int32_t* last_page_len, int B, int P, int32_t* kv_len)
+{
+    for (int b = 0; b < B; ++b) {
+        int64_t pages = (int64_t)indptr[b + 1] - indptr[b];
+        if (pages < 0 || indptr[b] < 0) {
+            kv_len[b] = -1;
+        } else if (pages == 0) {
+            kv_len[b] = 0;
+        } else {
+            int last = last_page_len[b];
+            kv_len[b] = (last < 1 || last > P) ? -1 : (int32_t)((pages - 1) * P + last);
+        }
+    }
+}
+
+/*
+ * Gather through the ragged page table: token t of request b lives on page
+ * indices[indptr[b] + t / P], slot t % P; the first kv_len(b) tokens go to
+ * out[(cum_kv[b] + t) * Hkv * D + h * D + d] (raw element bytes).  Returns 0,
+ * or -1 if a request is malformed or a page id is outside the pool.
+ */
+int oracle_gather_ragged(const oracle_pool* pool, int layout, const int32_t* indices, const int32_t* indptr,
+                         const int32_t* last_page_len, const int32_t* cum_kv, int B, void* out)
+{
+    int Hkv = pool_kv_heads(pool, layout);
+    int D = (int)pool->shape[3];
+    int P = pool_page_size(pool, layout);
+    int esize = pool->dtype == OR_BF16 ? 2 : 1;
+    int bad = 0;
+    int32_t* kv_len = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    oracle_ragged_lengths(indptr, last_page_len, B, P, kv_len);
+    for (int b = 0; b < B; ++b) {
+        if (kv_len[b] < 0) {
+            bad = 1;
+            continue;
+        }
+        for (int64_t t = 0; t < kv_len[b]; ++t) {
+            int32_t page = indices[indptr[b] + t / P];
+            for (int h = 0; h < Hkv; ++h) {
+                for (int d = 0; d < D; ++d) {
+                    int64_t dst = ((int64_t)cum_kv[b] + t) * Hkv * D + (int64_t)h * D + d;
+                    if (page < 0 || page >= pool->shape[0]) {
+                        bad = 1;
+                        memset((char*)out + dst * esize, 0, esize);
+                        continue;
+                    }
+                    int64_t src = pool_offset(pool, layout, page, h, t % P, d);
+                    memcpy((char*)out + dst * esize, (const char*)pool->data + src * esize, esize);
+                }
+            }
+        }
+    }
+    free(kv_len);
+    return bad ? -1 : 0;
+}
+
+/*
  * Attention for a list of output rows.
  *
  * rows[r] = token * H + h selects output row r (rows == NULL: every row in

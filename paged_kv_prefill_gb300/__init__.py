@@ -42,6 +42,8 @@ EXPORTED = [
     "b2pa_context_attention",
     "b2pa_context_attention_tensor_scales",
     "b2pa_batch_decode",
+    "b2pa_context_attention_ragged",
+    "b2pa_debug_gather_ragged",
     "b2pa_context_attention_noalloc",
     "b2pa_debug_worklist",
     "b2pa_debug_gather",
@@ -94,6 +96,12 @@ def load(path: str = LIB_PATH):
     lib.b2pa_batch_decode.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_int32, P, ctypes.c_int32, P, ctypes.c_void_p]
     lib.b2pa_batch_decode.restype = ctypes.c_int
+    lib.b2pa_context_attention_ragged.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
+                                                  ctypes.c_float, ctypes.c_float, ctypes.c_int32, P, ctypes.c_int32,
+                                                  P, ctypes.c_void_p]
+    lib.b2pa_context_attention_ragged.restype = ctypes.c_int
+    lib.b2pa_debug_gather_ragged.argtypes = [P, P, P, P, P, P, ctypes.c_int32, P, P, ctypes.c_void_p]
+    lib.b2pa_debug_gather_ragged.restype = ctypes.c_int
     lib.b2pa_context_attention_noalloc.argtypes = [P, P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
                                                    ctypes.c_float, ctypes.c_float, ctypes.c_int32, P,
                                                    ctypes.c_int32, P, ctypes.c_void_p, ctypes.c_void_p]
@@ -260,6 +268,44 @@ def batch_decode(
     return out
 
 
+def context_attention_ragged(
+    query: torch.Tensor,
+    kv_cache: Union[torch.Tensor, Sequence[torch.Tensor]],
+    paged_kv_indices: torch.Tensor,
+    paged_kv_indptr: torch.Tensor,
+    paged_kv_last_page_len: torch.Tensor,
+    max_q_len: int,
+    max_kv_len: int,
+    bmm1_scale: float,
+    bmm2_scale: float,
+    cum_seq_lens_q: torch.Tensor,
+    window_left: int = -1,
+    out: Optional[torch.Tensor] = None,
+    kv_layout: str = "HND",
+    sinks: Optional[torch.Tensor] = None,
+    stream=None,
+) -> torch.Tensor:
+    """context_attention with FlashInfer's ragged page table (flat page ids, their
+    per-request offsets and the valid tokens of each last page) in place of
+    block_tables and seq_lens (see include/b2pa.h)."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    if out is None:
+        out = torch.empty_like(query)
+    if isinstance(sinks, (list, tuple)):
+        if len(sinks) != 1:
+            raise ValueError("sinks: one fp32 [num_heads] tensor")
+        sinks = sinks[0]
+    d = [desc(x) for x in (query, k, v, paged_kv_indices, paged_kv_indptr, paged_kv_last_page_len, cum_seq_lens_q)]
+    dsk, do = desc(sinks), desc(out)
+    st = lib.b2pa_context_attention_ragged(
+        *(ctypes.byref(x) for x in d), int(max_q_len), int(max_kv_len), float(bmm1_scale), float(bmm2_scale),
+        int(window_left), _ref(dsk), LAYOUTS[kv_layout], ctypes.byref(do), ctypes.c_void_p(_stream_handle(stream)),
+    )
+    _check(st, "b2pa_context_attention_ragged")
+    return out
+
+
 def context_attention_noalloc(
     query: torch.Tensor,
     kv_cache: Union[torch.Tensor, Sequence[torch.Tensor]],
@@ -341,6 +387,23 @@ def debug_gather(kv_cache, block_tables, seq_lens, cum_seq_lens_kv, total_rows: 
     st = lib.b2pa_debug_gather(*(ctypes.byref(x) for x in d), LAYOUTS[kv_layout], ctypes.byref(dko),
                                ctypes.byref(dvo), ctypes.c_void_p(_stream_handle(stream)))
     _check(st, "b2pa_debug_gather")
+    return k_out, v_out
+
+
+def debug_gather_ragged(kv_cache, paged_kv_indices, paged_kv_indptr, paged_kv_last_page_len, cum_seq_lens_kv,
+                        total_rows: int, kv_layout="HND", stream=None):
+    """debug_gather for the ragged page table."""
+    lib = load()
+    k, v = split_kv_cache(kv_cache, kv_layout)
+    Hkv = k.shape[1] if kv_layout == "HND" else k.shape[2]
+    D = k.shape[3]
+    k_out = torch.zeros((total_rows, Hkv, D), dtype=k.dtype, device=k.device)
+    v_out = torch.zeros_like(k_out)
+    d = [desc(x) for x in (k, v, paged_kv_indices, paged_kv_indptr, paged_kv_last_page_len, cum_seq_lens_kv)]
+    dko, dvo = desc(k_out), desc(v_out)
+    st = lib.b2pa_debug_gather_ragged(*(ctypes.byref(x) for x in d), LAYOUTS[kv_layout], ctypes.byref(dko),
+                                      ctypes.byref(dvo), ctypes.c_void_p(_stream_handle(stream)))
+    _check(st, "b2pa_debug_gather_ragged")
     return k_out, v_out
 
 

@@ -239,7 +239,6 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     const uint32_t q_smem = smem_u32(c.base + C::kOffQ);
     const uint32_t ring = smem_u32(c.base + (FP8 ? C::kOffF8 : C::kOffRing));
     const int P = p.page_size;
-    const int ppt = P >= kKvTile ? 1 : kKvTile / P;  // pages per kv tile
     const int log2_p = 31 - __clz(P);                 // the tensor-core path takes powers of two only
     const int box_rows = P >= kKvTile ? kKvTile : P;
     const uint32_t q_box_bytes = (uint32_t)(p.G * p.rows_per_tile * 128);
@@ -307,14 +306,12 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             tma_load_3d(q_smem + (qb * kQTiles + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
                         h * 64, it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
         }
-        const int* bt_row = p.block_tables + (long long)it.b * p.bt_stride;
+        const int* bt_row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, it.b);
         const int n_pages_valid = (it.kv_len + P - 1) >> log2_p;
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
-            const int first_col = (int)(((long long)j * kKvTile) >> log2_p);
-            const int slot0 = P > kKvTile ? (int)(((long long)j * kKvTile) & (P - 1)) : 0;
-            const int col = first_col + lane;
-            const bool valid = lane < ppt && col < n_pages_valid;
-            const int page = valid ? bt_row[col] : 0;
+            const TileLoad tl = tile_load(bt_row, j, lane, log2_p, n_pages_valid);
+            const int slot0 = tl.slot0, page = tl.page;
+            const bool valid = tl.valid;
             if (valid && (page < 0 || page >= p.num_pages))
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
             const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));

@@ -195,6 +195,8 @@ struct Problem {
     const void *q, *k, *v;
     const int *bt, *seq, *cum_q, *cum_kv;
     int q_per_req;  // > 0: decode batch, request b owns query rows b * q_per_req .. (cum_q null)
+    const int* kv_indptr;      // ragged page table: bt = the flat page ids, seq = derived on the device
+    const int* last_page_len;
     const float* sinks;
     void* out;
 };
@@ -237,7 +239,8 @@ int parse_pools(const b2pa_tensor* k, const b2pa_tensor* v, int32_t layout, Prob
 int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                   const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens, const b2pa_tensor* cum_q,
                   const b2pa_tensor* cum_kv, const b2pa_tensor* sinks, int32_t layout, const b2pa_tensor* out,
-                  Problem* pr, int32_t q_per_req = 0)
+                  Problem* pr, int32_t q_per_req = 0, const b2pa_tensor* kv_indptr = nullptr,
+                  const b2pa_tensor* last_page_len = nullptr)
 {
     std::memset(pr, 0, sizeof *pr);
     int st = parse_pools(k_pool, v_pool, layout, pr);
@@ -266,14 +269,39 @@ int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_te
     pr->out_st_tok = out->stride[0];
     pr->out_st_head = out->stride[1];
     pr->out = out->data;
-    if (!seq_lens || seq_lens->ndim != 1)
-        return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be 1-D int32 [B]");
-    const int64_t B = seq_lens->shape[0];
-    if (B < 0 || B > 0x7FFFFFF)
-        return fail(B2PA_ERR_INVALID_ARG, "batch size");
-    pr->B = (int)B;
-    if (B > 0 && !is_vec(seq_lens, B2PA_INT32, B))
-        return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
+    int64_t B = 0;
+    if (kv_indptr != nullptr) {
+        // ragged page table: paged_kv_indptr [B + 1], paged_kv_last_page_len [B],
+        // block_tables = paged_kv_indices, the flat page ids [nnz]
+        if (kv_indptr->ndim != 1 || kv_indptr->shape[0] < 1)
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indptr must be 1-D int32 [B + 1]");
+        B = kv_indptr->shape[0] - 1;
+        if (B > 0x7FFFFFF || !is_vec(kv_indptr, B2PA_INT32, B + 1))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indptr must be contiguous int32 [B + 1]");
+        if (B > 0 && !is_vec(last_page_len, B2PA_INT32, B))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_last_page_len must be contiguous int32 [B]");
+        if (!block_tables || block_tables->ndim != 1 || block_tables->dtype != B2PA_INT32 ||
+            block_tables->shape[0] < 0 || block_tables->shape[0] > 0x7FFFFFFF ||
+            (block_tables->shape[0] > 1 && block_tables->stride[0] != 1))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indices must be contiguous int32 [nnz]");
+        if (block_tables->shape[0] > 0 && !block_tables->data)
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indices: null");
+        pr->kv_indptr = static_cast<const int*>(kv_indptr->data);
+        pr->last_page_len = B > 0 ? static_cast<const int*>(last_page_len->data) : nullptr;
+        pr->max_pages = 0x7FFFFFFF;  // each request's page count comes from the indptr
+        pr->bt_stride = 0;
+        pr->bt = static_cast<const int*>(block_tables->data);
+        pr->B = (int)B;
+    } else {
+        if (!seq_lens || seq_lens->ndim != 1)
+            return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be 1-D int32 [B]");
+        B = seq_lens->shape[0];
+        if (B < 0 || B > 0x7FFFFFF)
+            return fail(B2PA_ERR_INVALID_ARG, "batch size");
+        pr->B = (int)B;
+        if (B > 0 && !is_vec(seq_lens, B2PA_INT32, B))
+            return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
+    }
     if (q_per_req > 0) {
         if ((long long)B * q_per_req != (long long)pr->T)
             return fail(B2PA_ERR_INVALID_ARG, "q must hold batch x q_len_per_req = %lld x %d tokens, not %d",
@@ -283,16 +311,18 @@ int parse_problem(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_te
     }
     if (cum_kv && !is_vec(cum_kv, B2PA_INT32, B + 1))
         return fail(B2PA_ERR_INVALID_ARG, "cum_kv must be contiguous int32 [B + 1] (or NULL)");
-    if (!block_tables || block_tables->ndim != 2 || block_tables->dtype != B2PA_INT32 ||
-        block_tables->shape[0] != B || block_tables->shape[1] < 0 ||
-        (block_tables->shape[1] > 1 && block_tables->stride[1] != 1) || block_tables->shape[1] > 0x7FFFFFFF)
-        return fail(B2PA_ERR_INVALID_ARG, "block_tables must be int32 [B, max_pages] with unit column stride");
-    if (B > 0 && block_tables->shape[1] > 0 && !block_tables->data)
-        return fail(B2PA_ERR_INVALID_ARG, "block_tables: null");
-    pr->max_pages = (int)block_tables->shape[1];
-    pr->bt_stride = block_tables->stride[0];
-    pr->bt = static_cast<const int*>(block_tables->data);
-    pr->seq = static_cast<const int*>(B > 0 ? seq_lens->data : nullptr);
+    if (kv_indptr == nullptr) {
+        if (!block_tables || block_tables->ndim != 2 || block_tables->dtype != B2PA_INT32 ||
+            block_tables->shape[0] != B || block_tables->shape[1] < 0 ||
+            (block_tables->shape[1] > 1 && block_tables->stride[1] != 1) || block_tables->shape[1] > 0x7FFFFFFF)
+            return fail(B2PA_ERR_INVALID_ARG, "block_tables must be int32 [B, max_pages] with unit column stride");
+        if (B > 0 && block_tables->shape[1] > 0 && !block_tables->data)
+            return fail(B2PA_ERR_INVALID_ARG, "block_tables: null");
+        pr->max_pages = (int)block_tables->shape[1];
+        pr->bt_stride = block_tables->stride[0];
+        pr->bt = static_cast<const int*>(block_tables->data);
+    }
+    pr->seq = (kv_indptr == nullptr && B > 0) ? static_cast<const int*>(seq_lens->data) : nullptr;
     pr->cum_q = q_per_req > 0 ? nullptr : static_cast<const int*>(cum_q->data);
     pr->q_per_req = q_per_req > 0 ? q_per_req : 0;
     pr->cum_kv = cum_kv ? static_cast<const int*>(cum_kv->data) : nullptr;
@@ -437,6 +467,7 @@ int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, s
     ap->q_per_req = pr.q_per_req;
     ap->seq_lens = pr.seq;
     ap->block_tables = pr.bt;
+    ap->kv_indptr = pr.kv_indptr;
     ap->sinks = pr.sinks;
     ap->out = static_cast<uint16_t*>(pr.out);
     ap->bt_stride = pr.bt_stride;
@@ -505,6 +536,7 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     sp.cum_q = pr.cum_q;
     sp.q_per_req = pr.q_per_req;
     sp.seq_lens = pr.seq;
+    sp.kv_indptr = pr.kv_indptr;
     sp.cum_kv = pr.cum_kv;
     sp.block_tables = pr.bt;
     sp.bt_stride = pr.bt_stride;
@@ -569,11 +601,12 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
                            const b2pa_tensor* cum_kv, int32_t max_q_len, int32_t max_kv_len, float bmm1_scale,
                            float bmm2_scale, const float* bmm1_dev, const float* bmm2_dev, int32_t window_left,
                            const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out, cudaStream_t stream,
-                           int32_t q_per_req = 0)
+                           int32_t q_per_req = 0, const b2pa_tensor* kv_indptr = nullptr,
+                           const b2pa_tensor* last_page_len = nullptr)
 {
     Problem pr;
     int st = parse_problem(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, sinks, layout, out, &pr,
-                           q_per_req);
+                           q_per_req, kv_indptr, last_page_len);
     if (st)
         return st;
     if (max_q_len < 0 || max_kv_len < 0)
@@ -598,10 +631,21 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         const size_t off_nsplit = kWsHeader + cap * sizeof(int4);
         const size_t off_ml = (off_nsplit + (size_t)pr.B * sizeof(int) + 255) / 256 * 256;
         const size_t off_o = (off_ml + rows * 2 * sizeof(float) + 255) / 256 * 256;
-        const size_t need = split.split_tiles > 0 ? off_o + rows * pr.D * sizeof(float) : off_nsplit;
+        const size_t body = split.split_tiles > 0 ? off_o + rows * pr.D * sizeof(float) : off_nsplit;
+        // ragged page table: the kv lengths derived on the device, last
+        const size_t off_seq = (body + 255) / 256 * 256;
+        const size_t need = pr.kv_indptr ? off_seq + (size_t)pr.B * sizeof(int) : body;
         Workspace ws;
         if ((st = get_workspace_bytes(dev, stream, need, &ws)))
             return st;
+        if (pr.kv_indptr) {
+            int* kv_len = reinterpret_cast<int*>(ws.mem + off_seq);
+            cudaError_t e = launch_ragged_lengths(pr.kv_indptr, pr.last_page_len, pr.B, pr.P, kv_len,
+                                                  reinterpret_cast<unsigned*>(ws.mem), stream);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "ragged page-table lengths launch");
+            pr.seq = kv_len;
+        }
         SchedParams sp = make_sched(pr, ws, max_q_len, max_kv_len, window, cap);
         AttnParams ap;
         // a shape the tensor-core path accepts must encode; a failure is an
@@ -655,8 +699,16 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         return B2PA_OK;
     }
     Workspace ws;
-    if ((st = get_workspace(dev, stream, 1, &ws)))
+    if ((st = get_workspace_bytes(dev, stream, kWsHeader + (size_t)pr.B * sizeof(int), &ws)))
         return st;
+    if (pr.kv_indptr) {
+        int* kv_len = reinterpret_cast<int*>(ws.mem + kWsHeader);
+        cudaError_t e = launch_ragged_lengths(pr.kv_indptr, pr.last_page_len, pr.B, pr.P, kv_len,
+                                              reinterpret_cast<unsigned*>(ws.mem), stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "ragged page-table lengths launch");
+        pr.seq = kv_len;
+    }
     GenericParams gp;
     std::memset(&gp, 0, sizeof gp);
     gp.q = static_cast<const uint16_t*>(pr.q);
@@ -666,6 +718,7 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     gp.q_per_req = pr.q_per_req;
     gp.seq_lens = pr.seq;
     gp.block_tables = pr.bt;
+    gp.kv_indptr = pr.kv_indptr;
     gp.sinks = pr.sinks;
     gp.out = static_cast<uint16_t*>(pr.out);
     gp.q_st_tok = pr.q_st_tok;
@@ -717,6 +770,22 @@ int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
     return context_attention_impl(q, k_pool, v_pool, block_tables, seq_lens, cum_q, cum_kv, max_q_len, max_kv_len,
                                   bmm1_scale, bmm2_scale, nullptr, nullptr, window_left, sinks, layout, out,
                                   reinterpret_cast<cudaStream_t>(stream_h));
+}
+
+int b2pa_context_attention_ragged(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                                  const b2pa_tensor* paged_kv_indices, const b2pa_tensor* paged_kv_indptr,
+                                  const b2pa_tensor* paged_kv_last_page_len, const b2pa_tensor* cum_q,
+                                  int32_t max_q_len, int32_t max_kv_len, float bmm1_scale, float bmm2_scale,
+                                  int32_t window_left, const b2pa_tensor* sinks, int32_t layout, b2pa_tensor* out,
+                                  b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    if (!paged_kv_indptr)
+        return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indptr: null");
+    return context_attention_impl(q, k_pool, v_pool, paged_kv_indices, nullptr, cum_q, nullptr, max_q_len, max_kv_len,
+                                  bmm1_scale, bmm2_scale, nullptr, nullptr, window_left, sinks, layout, out,
+                                  reinterpret_cast<cudaStream_t>(stream_h), 0, paged_kv_indptr,
+                                  paged_kv_last_page_len);
 }
 
 int b2pa_batch_decode(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
@@ -806,25 +875,44 @@ int b2pa_debug_worklist(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b
     return B2PA_OK;
 }
 
-int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
-                      const b2pa_tensor* seq_lens, const b2pa_tensor* cum_kv, int32_t layout, b2pa_tensor* k_out,
-                      b2pa_tensor* v_out, b2pa_stream_t stream_h)
+}  // extern "C"
+
+namespace {
+
+// Both debug gathers: a [B, max_pages] block table with seq_lens, or the
+// ragged page table (kv_indptr non-null; block_tables = the flat page ids).
+int debug_gather_impl(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
+                      const b2pa_tensor* seq_lens, const b2pa_tensor* kv_indptr, const b2pa_tensor* last_page_len,
+                      const b2pa_tensor* cum_kv, int32_t layout, b2pa_tensor* k_out, b2pa_tensor* v_out,
+                      cudaStream_t stream)
 {
-    g_last_error.clear();
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
     Problem pr;
     std::memset(&pr, 0, sizeof pr);
     int st = parse_pools(k_pool, v_pool, layout, &pr);
     if (st)
         return st;
-    if (!seq_lens || seq_lens->ndim != 1)
-        return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be 1-D int32 [B]");
-    const int64_t B = seq_lens->shape[0];
-    if (B < 0 || B > 0x7FFFFFF || (B > 0 && !is_vec(seq_lens, B2PA_INT32, B)) || !is_vec(cum_kv, B2PA_INT32, B + 1))
-        return fail(B2PA_ERR_INVALID_ARG, "seq_lens [B] / cum_kv [B + 1] must be contiguous int32");
-    if (!block_tables || block_tables->ndim != 2 || block_tables->dtype != B2PA_INT32 ||
-        block_tables->shape[0] != B || (block_tables->shape[1] > 1 && block_tables->stride[1] != 1))
-        return fail(B2PA_ERR_INVALID_ARG, "block_tables must be int32 [B, max_pages]");
+    int64_t B = 0;
+    if (kv_indptr != nullptr) {
+        if (kv_indptr->ndim != 1 || kv_indptr->shape[0] < 1 || kv_indptr->shape[0] - 1 > 0x7FFFFFF ||
+            !is_vec(kv_indptr, B2PA_INT32, kv_indptr->shape[0]))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indptr must be contiguous int32 [B + 1]");
+        B = kv_indptr->shape[0] - 1;
+        if ((B > 0 && !is_vec(last_page_len, B2PA_INT32, B)) || !is_vec(cum_kv, B2PA_INT32, B + 1))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_last_page_len [B] / cum_kv [B + 1] must be contiguous int32");
+        if (!block_tables || block_tables->ndim != 1 || block_tables->dtype != B2PA_INT32 ||
+            (block_tables->shape[0] > 1 && block_tables->stride[0] != 1))
+            return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indices must be contiguous int32 [nnz]");
+    } else {
+        if (!seq_lens || seq_lens->ndim != 1)
+            return fail(B2PA_ERR_INVALID_ARG, "seq_lens must be 1-D int32 [B]");
+        B = seq_lens->shape[0];
+        if (B < 0 || B > 0x7FFFFFF || (B > 0 && !is_vec(seq_lens, B2PA_INT32, B)) ||
+            !is_vec(cum_kv, B2PA_INT32, B + 1))
+            return fail(B2PA_ERR_INVALID_ARG, "seq_lens [B] / cum_kv [B + 1] must be contiguous int32");
+        if (!block_tables || block_tables->ndim != 2 || block_tables->dtype != B2PA_INT32 ||
+            block_tables->shape[0] != B || (block_tables->shape[1] > 1 && block_tables->stride[1] != 1))
+            return fail(B2PA_ERR_INVALID_ARG, "block_tables must be int32 [B, max_pages]");
+    }
     const int dt = k_pool->dtype;
     for (const b2pa_tensor* o : {static_cast<const b2pa_tensor*>(k_out), static_cast<const b2pa_tensor*>(v_out)}) {
         if (!o || !o->data || o->ndim != 3 || o->dtype != dt || o->shape[1] != pr.Hkv || o->shape[2] != pr.D ||
@@ -834,8 +922,8 @@ int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, cons
     if (k_out->shape[0] != v_out->shape[0])
         return fail(B2PA_ERR_INVALID_ARG, "k_out and v_out rows differ");
     pr.B = (int)B;
-    pr.max_pages = (int)block_tables->shape[1];
-    pr.bt_stride = block_tables->stride[0];
+    pr.max_pages = kv_indptr ? 0x7FFFFFFF : (int)block_tables->shape[1];
+    pr.bt_stride = kv_indptr ? 0 : block_tables->stride[0];
     // borrow the tensor-core checks with q/out stand-ins that always pass
     static const uint4 dummy = {0, 0, 0, 0};
     pr.q = &dummy;
@@ -850,13 +938,24 @@ int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, cons
     if (B == 0)
         return B2PA_OK;
     Workspace ws;
-    if ((st = get_workspace(dev, stream, 1, &ws)))
+    if ((st = get_workspace_bytes(dev, stream, kWsHeader + (size_t)B * sizeof(int), &ws)))
         return st;
     GatherParams gp;
     std::memset(&gp, 0, sizeof gp);
     if ((st = encode_pool_map(&gp.tm_k, pr, pr.k, pr.k_st)) || (st = encode_pool_map(&gp.tm_v, pr, pr.v, pr.v_st)))
         return st;
-    gp.seq_lens = static_cast<const int*>(seq_lens->data);
+    if (kv_indptr != nullptr) {
+        int* kv_len = reinterpret_cast<int*>(ws.mem + kWsHeader);
+        cudaError_t e = launch_ragged_lengths(static_cast<const int*>(kv_indptr->data),
+                                              static_cast<const int*>(last_page_len->data), (int)B, pr.P, kv_len,
+                                              reinterpret_cast<unsigned*>(ws.mem), stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "ragged page-table lengths launch");
+        gp.seq_lens = kv_len;
+        gp.kv_indptr = static_cast<const int*>(kv_indptr->data);
+    } else {
+        gp.seq_lens = static_cast<const int*>(seq_lens->data);
+    }
     gp.cum_kv = static_cast<const int*>(cum_kv->data);
     gp.block_tables = static_cast<const int*>(block_tables->data);
     gp.bt_stride = pr.bt_stride;
@@ -876,6 +975,31 @@ int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, cons
     if (e != cudaSuccess)
         return cuda_fail(e, "gather launch");
     return B2PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int b2pa_debug_gather(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool, const b2pa_tensor* block_tables,
+                      const b2pa_tensor* seq_lens, const b2pa_tensor* cum_kv, int32_t layout, b2pa_tensor* k_out,
+                      b2pa_tensor* v_out, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    return debug_gather_impl(k_pool, v_pool, block_tables, seq_lens, nullptr, nullptr, cum_kv, layout, k_out, v_out,
+                             reinterpret_cast<cudaStream_t>(stream_h));
+}
+
+int b2pa_debug_gather_ragged(const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
+                             const b2pa_tensor* paged_kv_indices, const b2pa_tensor* paged_kv_indptr,
+                             const b2pa_tensor* paged_kv_last_page_len, const b2pa_tensor* cum_kv, int32_t layout,
+                             b2pa_tensor* k_out, b2pa_tensor* v_out, b2pa_stream_t stream_h)
+{
+    g_last_error.clear();
+    if (!paged_kv_indptr)
+        return fail(B2PA_ERR_INVALID_ARG, "paged_kv_indptr: null");
+    return debug_gather_impl(k_pool, v_pool, paged_kv_indices, nullptr, paged_kv_indptr, paged_kv_last_page_len,
+                             cum_kv, layout, k_out, v_out, reinterpret_cast<cudaStream_t>(stream_h));
 }
 
 int b2pa_append_kv(const b2pa_tensor* k_new, const b2pa_tensor* v_new, const b2pa_tensor* k_pool,

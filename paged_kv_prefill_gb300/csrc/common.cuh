@@ -77,6 +77,38 @@ __device__ __forceinline__ ItemGeom item_geometry(int q_len, int kv_len, int it,
     return g;
 }
 
+// The page ids of request b: a row of a [B, max_pages] block table, or (the
+// ragged form) the slice ids[indptr[b] .. indptr[b + 1]) of one flat array
+// (FlashInfer's paged_kv_indices / paged_kv_indptr).
+__device__ __forceinline__ const int* page_row(const int* ids, long long row_stride, const int* indptr, int b)
+{
+    return indptr != nullptr ? ids + indptr[b] : ids + (long long)b * row_stride;
+}
+
+// Kv tile j of a request as per-page TMA boxes, for page sizes that are
+// powers of two: lane l of a warp loads page column (j * kKvTile >> log2 P) + l,
+// from in-page slot slot0 (nonzero only when P > kKvTile).  A lane is valid if
+// l < pages per tile and its column is below the request's page count.  The
+// attention producer and the debug gather both address pages through this.
+struct TileLoad {
+    int page;
+    int slot0;
+    bool valid;
+};
+
+__device__ __forceinline__ TileLoad tile_load(const int* row, int j, int lane, int log2_p, int n_pages)
+{
+    const int P = 1 << log2_p;
+    const int ppt = P >= kKvTile ? 1 : kKvTile >> log2_p;  // pages per kv tile
+    TileLoad t;
+    const int first_col = (int)(((long long)j * kKvTile) >> log2_p);
+    t.slot0 = P > kKvTile ? (int)(((long long)j * kKvTile) & (P - 1)) : 0;
+    const int col = first_col + lane;
+    t.valid = lane < ppt && col < n_pages;
+    t.page = t.valid ? row[col] : 0;
+    return t;
+}
+
 // Split-KV (decode batches): a request's single work item per kv head is cut
 // into chunks of `split_tiles` kv tiles; chunk s covers tiles
 // n_lo + s * split_tiles .. (clipped to n_hi).
@@ -118,6 +150,7 @@ __device__ __forceinline__ Scales load_scales(float scale_log2, float bmm2, cons
 struct SchedParams {
     const int* cum_q;         // null: q_per_req query tokens per request (decode batch)
     int q_per_req;
+    const int* kv_indptr;     // non-null: ragged page table (block_tables = the flat page ids)
     const int* seq_lens;
     const int* cum_kv;        // may be null
     const int* block_tables;  // read only when debug != 0
@@ -144,6 +177,7 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     int q_per_req;
     const int* seq_lens;
     const int* block_tables;
+    const int* kv_indptr;  // non-null: ragged page table (block_tables = the flat page ids)
     const float* sinks;  // may be null
     uint16_t* out;       // bf16 bits
     int split_tiles;     // > 0: items are kv chunks; a chunk of a request cut in several writes partials
@@ -172,6 +206,7 @@ struct GatherParams {
     const int* seq_lens;
     const int* cum_kv;
     const int* block_tables;
+    const int* kv_indptr;  // non-null: ragged page table
     long long bt_stride;
     uint8_t* k_out;
     uint8_t* v_out;
@@ -188,6 +223,7 @@ struct GenericParams {
     int q_per_req;
     const int* seq_lens;
     const int* block_tables;
+    const int* kv_indptr;  // non-null: ragged page table
     const float* sinks;
     uint16_t* out;
     long long q_st_tok, q_st_head;
@@ -223,5 +259,9 @@ cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int
 cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaStream_t stream);
 cudaError_t launch_attention_generic(const GenericParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+// Ragged page table: kv_len[b] = (pages_b - 1) * page_size + last_page_len[b]
+// (0 without pages); a malformed request gets kv_len -1 and B2PA_DEV_BAD_REQUEST.
+cudaError_t launch_ragged_lengths(const int* indptr, const int* last_page_len, int B, int page_size, int* kv_len,
+                                  unsigned* err, cudaStream_t stream);
 
 }  // namespace b2pa

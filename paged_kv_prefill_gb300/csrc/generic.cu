@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kGenericWarps * 32) generic_attention_kernel(c
     for (int k = 0; k < kPer; ++k)
         o[k] = 0.f;
     float m = -INFINITY, l = 0.f;
-    const int* bt_row = p.block_tables + (long long)b * p.bt_stride;
+    const int* bt_row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, b);
 
     for (int base = lo; base <= pos; base += 32) {
         const int key = base + lane;

@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedP
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_CUM_KV);
             if (r.ok) {
                 const int pages = (r.kv_len + p.page_size - 1) / p.page_size;
+                const int* row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, b);
                 for (int col = 0; col < pages; ++col) {
-                    const int id = p.block_tables[(long long)b * p.bt_stride + col];
+                    const int id = row[col];
                     if (id < 0 || id >= p.num_pages)
                         atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
                 }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(128) gather_kernel(const __grid_constant__ Gat
     if (kv_len < 0 || (long long)j * kKvTile >= kv_len)
         return;
     const int P = p.page_size;
-    if ((kv_len + P - 1) / P > p.max_pages) {
+    if (p.kv_indptr == nullptr && (kv_len + P - 1) / P > p.max_pages) {
         if (threadIdx.x == 0)
             atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
         return;
@@ -314,16 +315,16 @@ __global__ void __launch_bounds__(128) gather_kernel(const __grid_constant__ Gat
     }
     __syncthreads();
     const int rows = min(kKvTile, kv_len - j * kKvTile);
-    const int ppt = P >= kKvTile ? 1 : kKvTile / P;
     const int box_rows = P >= kKvTile ? kKvTile : P;
+    const int log2_p = 31 - __clz(P);  // page sizes of the tensor-core loads are powers of two
+    const int* bt_row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, b);
     for (int kind = 0; kind < 2; ++kind) {
         if (threadIdx.x < 32) {
+            // the attention producer's page addressing
             const int lane = threadIdx.x;
-            const int first_col = (int)(((long long)j * kKvTile) / P);
-            const int slot0 = P > kKvTile ? (int)(((long long)j * kKvTile) % P) : 0;
-            const int col = first_col + lane;
-            const bool valid = lane < ppt && col < (kv_len + P - 1) / P;
-            const int page = valid ? p.block_tables[(long long)b * p.bt_stride + col] : 0;
+            const TileLoad tl = tile_load(bt_row, j, lane, log2_p, (kv_len + P - 1) >> log2_p);
+            const int slot0 = tl.slot0, page = tl.page;
+            const bool valid = tl.valid;
             if (valid && (page < 0 || page >= p.num_pages))
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
             const uint32_t nvalid = __popc(__ballot_sync(0xffffffffu, valid));
@@ -370,6 +371,45 @@ cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaS
     if (e != cudaSuccess)
         return e;
     kern<<<dim3(tiles, p.Hkv, p.B), 128, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace b2pa
+
+namespace b2pa {
+
+// ---------------------------------------------------------------------------
+// Ragged page table (FlashInfer's paged_kv_indices / paged_kv_indptr /
+// paged_kv_last_page_len): each request's kv length from its page count and
+// the valid tokens of its last page.  A request with a negative page count, or
+// with pages and a last_page_len outside [1, page_size], is malformed: its
+// length becomes -1, which every later check rejects.
+// ---------------------------------------------------------------------------
+__global__ void ragged_lengths_kernel(const int* indptr, const int* last, int B, int P, int* kv_len, unsigned* err)
+{
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+        const int pages = indptr[b + 1] - indptr[b];
+        int len = 0;
+        if (pages < 0 || indptr[b] < 0) {
+            len = -1;
+        } else if (pages > 0) {
+            const int lp = last[b];
+            len = (lp < 1 || lp > P) ? -1 : (int)min((long long)(pages - 1) * P + lp, 0x7FFFFFFFLL);
+        }
+        if (len < 0)
+            atomicOr(err, (unsigned)B2PA_DEV_BAD_REQUEST);
+        kv_len[b] = len;
+    }
+}
+
+cudaError_t launch_ragged_lengths(const int* indptr, const int* last_page_len, int B, int page_size, int* kv_len,
+                                  unsigned* err, cudaStream_t stream)
+{
+    if (B == 0)
+        return cudaSuccess;
+    const int blocks = (B + 255) / 256;
+    ragged_lengths_kernel<<<blocks < 64 ? blocks : 64, 256, 0, stream>>>(indptr, last_page_len, B, page_size, kv_len,
+                                                                           err);
     return cudaGetLastError();
 }
 

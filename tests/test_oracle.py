@@ -319,6 +319,59 @@ def test_gather_flags_out_of_pool_ids():
     assert not ok
 
 
+# ---------------------------------------------------------------- ragged page table
+
+def test_ragged_lengths_hand_cases():
+    """kv length = (pages - 1) * P + last_page_len, 0 without pages, -1 if malformed."""
+    ip = torch.tensor([0, 3, 4, 4, 6, 6, 7], dtype=torch.int32)
+    last = torch.tensor([1, 4, 9, 0, 2, 5], dtype=torch.int32)
+    assert oracle.ragged_lengths(ip, last, 4).tolist() == [9, 4, 0, -1, 0, -1]
+    assert oracle.ragged_lengths(torch.tensor([0, 2, 1], dtype=torch.int32), torch.tensor([1, 1], dtype=torch.int32),
+                                 4).tolist() == [5, -1]
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_gather_ragged_matches_torch_indexing(layout, dtype):
+    """Token t of request b from page indices[indptr[b] + t // P], slot t % P,
+    written out with torch advanced indexing."""
+    inp = _small(seed=19, layout=layout, kv_dtype=dtype, table_pad="garbage")
+    idx, ip, last = workload.ragged_page_table(inp)
+    P = inp.page_size
+    for which, pool in (("k", inp.k_pool), ("v", inp.v_pool)):
+        got, ok = oracle.gather_ragged(inp, idx, ip, last, which)
+        assert ok
+        for b in range(inp.batch):
+            n = int(ip[b + 1] - ip[b])
+            kl = (n - 1) * P + int(last[b]) if n > 0 else 0
+            c0 = int(inp.cum_kv[b])
+            t = torch.arange(kl)
+            pages = idx.long()[int(ip[b]) + t // P]
+            ref = pool[pages, :, t % P] if layout == "HND" else pool[pages, t % P]
+            assert torch.equal(got[c0:c0 + kl].view(torch.uint8), ref.contiguous().view(torch.uint8))
+
+
+def test_ragged_table_describes_the_same_attention():
+    """The ragged form of a batch's pages gives exactly the block-table form's output."""
+    inp = _small(seed=20, window_left=5, with_sinks=True)
+    idx, ip, last = workload.ragged_page_table(inp)
+    a, st_a, _ = oracle.attention(inp)
+    r, st_r, _ = oracle.attention_ragged(inp, idx, ip, last)
+    assert (st_a == 0).all() and (st_r == 0).all()
+    np.testing.assert_array_equal(a, r)
+
+
+def test_gather_ragged_flags_bad_tables():
+    inp = _small(seed=21)
+    idx, ip, last = workload.ragged_page_table(inp)
+    bad_last = last.clone()
+    bad_last[0] = inp.page_size + 1
+    assert not oracle.gather_ragged(inp, idx, ip, bad_last, "k")[1]
+    bad_idx = idx.clone()
+    bad_idx[0] = inp.k_pool.shape[0] + 3
+    assert not oracle.gather_ragged(inp, bad_idx, ip, last, "k")[1]
+
+
 # ---------------------------------------------------------------- work list
 
 def _brute_items(inp, rows_per_tile, nqt, bn):
@@ -520,6 +573,10 @@ _MUTANTS = {
     "append_unscaled": ("float q = x / scale;", "float q = x;"),
     # the write: slot within the page mirrored
     "append_slot": ("int64_t page = loc / P, slot = loc % P;", "int64_t page = loc / P, slot = (P - 1) - loc % P;"),
+    # ragged table: the last page counted as full
+    "ragged_last_full": ("(int32_t)((pages - 1) * P + last)", "(int32_t)(pages * P)"),
+    # ragged table: a request's pages taken from the next request's slice
+    "ragged_slice": ("int32_t page = indices[indptr[b] + t / P];", "int32_t page = indices[indptr[b + 1] - 1 - t / P];"),
 }
 
 
@@ -552,6 +609,8 @@ def _pins_pass(lib_path):
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_append_kv.restype = ctypes.c_int64
+        lib.oracle_gather_ragged.restype = ctypes.c_int
+        lib.oracle_ragged_lengths.restype = None
         oracle._lib = lib
         checks = [
             lambda: test_matches_torch_sdpa_fp64("HND", 3, True),
@@ -563,6 +622,8 @@ def _pins_pass(lib_path):
             lambda: test_e4m3_encoder_saturates_at_448(),
             lambda: test_append_matches_torch_indexing("NHD", True, (0.013, 0.004)),
             lambda: test_append_then_gather_returns_the_new_tokens("HND"),
+            lambda: test_ragged_lengths_hand_cases(),
+            lambda: test_gather_ragged_matches_torch_indexing("NHD", "bf16"),
         ]
         for c in checks:
             try:

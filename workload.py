@@ -323,3 +323,20 @@ def decode_config(q_len_per_req: int = 1, seed: Optional[int] = None, kv_dtype: 
     name = f"decode_b32_q{q_len_per_req}_kv-32768_h32kv8_d128_p32_hnd" + ("" if kv_dtype == "bf16" else "_fp8kv")
     return build([q_len_per_req] * 32, kv, 32, 8, 128, 32, "HND", kv_dtype=kv_dtype, pool_factor=2.0, seed=s,
                  name=name)
+
+
+def ragged_page_table(inp: Inputs):
+    """The same batch's pages as FlashInfer's ragged page table: the flat page ids
+    of every request (its first ceil(kv_len / P) block-table columns, in order),
+    their per-request offsets [B + 1], and the tokens in each request's last
+    page (P for a full page; 0 for a request without pages, where it is not
+    read).  Returns int32 tensors (indices, indptr, last_page_len)."""
+    P = inp.page_size
+    ids, indptr, last = [], [0], []
+    for b, L in enumerate(inp.kv_lens):
+        n = (L + P - 1) // P
+        ids.extend(inp.block_tables[b, :n].tolist())
+        indptr.append(indptr[-1] + n)
+        last.append(L - (n - 1) * P if n > 0 else 0)
+    return (torch.tensor(ids, dtype=torch.int32), torch.tensor(indptr, dtype=torch.int32),
+            torch.tensor(last, dtype=torch.int32))
