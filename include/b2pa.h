@@ -377,6 +377,23 @@ B2PA_API int b2pa_set_kernel_path(int32_t path);
 B2PA_API int b2pa_query_path(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                     const b2pa_tensor* out, int32_t layout);
 
+/* Failure detection (no counterpart on the pages): the longest a pipeline wait
+ * inside the tensor-core attention kernel may take, in ns of the GPU's global
+ * timer, for later calls in this process; 0 restores the default, 2 s.  A wait
+ * that runs out raises B2PA_DEV_TIMEOUT in the device error word: the CTA
+ * stops, lets its in-flight copies and MMAs finish (those drains keep the 2 s
+ * limit), frees its tensor memory and exits, so the context stays usable and
+ * the call's output is undefined.  Serving code leaves the default. */
+B2PA_API int b2pa_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Failure-detection tests (no counterpart on the pages): with on != 0, the
+ * attention kernels of later calls in this process make one pipeline wait on a
+ * barrier that nothing ever arrives on, so the wait limit runs out and every
+ * CTA takes the abort path described at b2pa_set_wait_limit_ns; 0 turns it
+ * off.  Nothing faults, traps or hangs: the call returns, the stream's device
+ * error word holds B2PA_DEV_TIMEOUT and the context stays usable. */
+B2PA_API int b2pa_debug_inject_stall(int32_t on);
+
 /* Turn on (1) / off (0) the extra device-side input checks: page ids against the pool and
  * cum_kv against seq_lens.  Off by default. */
 B2PA_API int b2pa_set_debug_checks(int32_t on);

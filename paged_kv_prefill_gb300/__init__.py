@@ -52,6 +52,8 @@ EXPORTED = [
     "b2pa_set_kernel_path",
     "b2pa_query_path",
     "b2pa_set_debug_checks",
+    "b2pa_set_wait_limit_ns",
+    "b2pa_debug_inject_stall",
     "b2pa_set_timing_events",
     "b2pa_status_string",
     "b2pa_last_error_message",
@@ -123,6 +125,10 @@ def load(path: str = LIB_PATH):
     lib.b2pa_set_timing_events.restype = ctypes.c_int
     lib.b2pa_set_debug_checks.argtypes = [ctypes.c_int32]
     lib.b2pa_set_debug_checks.restype = ctypes.c_int
+    lib.b2pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.b2pa_set_wait_limit_ns.restype = ctypes.c_int
+    lib.b2pa_debug_inject_stall.argtypes = [ctypes.c_int32]
+    lib.b2pa_debug_inject_stall.restype = ctypes.c_int
     lib.b2pa_status_string.argtypes = [ctypes.c_int32]
     lib.b2pa_status_string.restype = ctypes.c_char_p
     lib.b2pa_last_error_message.argtypes = []
@@ -448,6 +454,16 @@ def query_path(query, kv_cache, out=None, kv_layout="HND") -> str:
     if st < 0:
         _check(st, "b2pa_query_path")
     return {PATH_TCGEN05: "tcgen05", PATH_GENERIC: "generic"}[st]
+
+
+def set_wait_limit_ns(limit_ns: int):
+    """Longest pipeline wait inside the attention kernel (ns); 0 restores the 2 s default."""
+    _check(load().b2pa_set_wait_limit_ns(int(limit_ns)), "b2pa_set_wait_limit_ns")
+
+
+def debug_inject_stall(on: bool):
+    """Failure-detection tests: later attention kernels make one wait nothing completes (see include/b2pa.h)."""
+    _check(load().b2pa_debug_inject_stall(1 if on else 0), "b2pa_debug_inject_stall")
 
 
 def set_debug_checks(on: bool):

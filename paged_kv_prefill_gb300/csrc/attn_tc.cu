@@ -45,9 +45,11 @@
 // The row maximum of an S tile comes with its TMEM load (tcgen05.ld.red, an
 // sm_103a instruction) except on tiles that need masking.
 //
-// Every wait is bounded: after kWaitLimitNs (2 s of %globaltimer) the CTA raises
-// B2PA_DEV_TIMEOUT, every role leaves its loop, in-flight TMA copies and
-// MMAs are drained, and TMEM is freed before the CTA exits.
+// Every wait is bounded: after the call's wait limit (2 s of %globaltimer unless
+// b2pa_set_wait_limit_ns changed it) the CTA raises B2PA_DEV_TIMEOUT, every
+// role leaves its loop, in-flight TMA loads (K/V and Q), TMA stores and MMAs
+// are drained (those drains keep the 2 s limit), and TMEM is freed before the
+// CTA exits.
 #include <mutex>
 
 #include "common.cuh"
@@ -91,7 +93,7 @@ struct TcCfg {
     static constexpr int kOffBar = kOffStage + (kStageOut ? 8 * kStageWarpBytes : 0);
     // P_t is handed to the MMA warp in kPParts parts of kKvTile / kPParts keys
     static constexpr int kPParts = 1;
-    static constexpr int kNumBars = 4 * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots;
+    static constexpr int kNumBars = 4 * kPairs + 2 * kF8Stages + 3 * kQBufs + (2 + kPParts) * kQTiles + 1 + 2 * kItemSlots + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     // FP8: the power-of-two exponent of each Q row (int8), for the items of
     // both parities (a row's exponent is read by the softmax while the next
@@ -121,6 +123,7 @@ struct Bars {
     uint64_t* drain;
     uint64_t* it_full;   // [kItemSlots] item index posted
     uint64_t* it_empty;  // [kItemSlots] item index read by every consumer warp
+    uint64_t* never;     // [1]        nothing arrives: the injected stall of failure-detection tests
 };
 
 struct Ctx {
@@ -130,10 +133,19 @@ struct Ctx {
     int n_items;
     volatile int* item_slot;
     volatile int* abort_flag;
+    unsigned* err;
+    unsigned long long wait_limit_ns;  // a pipeline wait longer than this gives up
 };
 
-// Bounded wait on a barrier phase; false if this CTA gave up.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* err)
+// Bounded wait on a barrier phase; false if this CTA gave up (another role
+// raised the abort flag, or c.wait_limit_ns of %globaltimer passed: then this
+// wait raises it and sets B2PA_DEV_TIMEOUT).
+// Every caller is a whole warp.  The lanes of a converged warp see the same
+// barrier state, so they leave a satisfied wait together; giving up is decided
+// as a warp (a vote, taken only between unsuccessful tries), so that a lane
+// reading the timer a cycle later cannot split the warp before
+// warp-collective instructions (tcgen05.ld.sync.aligned, __syncwarp).
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctx& c)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity))
@@ -142,11 +154,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     while (true) {
         if (mbar_try_wait(a, parity))
             return true;
-        if (*abort_flag)
-            return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(err, (unsigned)B2PA_DEV_TIMEOUT);
+        const bool timed_out = global_ns() - t0 > c.wait_limit_ns;
+        if (__any_sync(0xffffffffu, *c.abort_flag != 0 || timed_out)) {
+            if (timed_out && (threadIdx.x & 31) == 0) {
+                *c.abort_flag = 1;
+                atomicOr(c.err, (unsigned)B2PA_DEV_TIMEOUT);
+            }
+            __syncwarp();
             return false;
         }
     }
@@ -199,7 +213,7 @@ template <int kSlots>
 __device__ __forceinline__ int take_item(const AttnParams& p, const Ctx& c, uint32_t n, bool* ok, ItemInfo* it)
 {
     const uint32_t s = n % kSlots;
-    if (!wait_bar(&c.bar.it_full[s], (n / kSlots) & 1, c.abort_flag, p.err)) {
+    if (!wait_bar(&c.bar.it_full[s], (n / kSlots) & 1, c)) {
         *ok = false;
         return -1;
     }
@@ -245,6 +259,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
 
     uint32_t ring_idx = 0;
     uint32_t ring_kv[2] = {0, 0};  // 16-bit path: K and V tiles whose copies were started
+    uint32_t q_loads = 0;          // items whose Q copies were started
     bool ok = true;
     // scales passed as device tensors are checked here: if they are unusable,
     // no item is taken, so every role finishes without writing anything
@@ -254,7 +269,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     for (uint32_t n = 0; ok; ++n) {
         // post the next item index
         const uint32_t slot = n % C::kItemSlots;
-        if (!wait_bar(&c.bar.it_empty[slot], ((n / C::kItemSlots) & 1) ^ 1, c.abort_flag, p.err))
+        if (!wait_bar(&c.bar.it_empty[slot], ((n / C::kItemSlots) & 1) ^ 1, c))
             break;
         volatile int* rec = c.item_slot + slot * kItemRecWords;
         if (lane == 0) {
@@ -296,7 +311,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         it.chunks = rec[11];
         // Q tiles, into the buffer of this item once its previous user is done
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
-        if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c.abort_flag, p.err))
+        if (!wait_bar(&c.bar.q_empty[qb], qph ^ 1, c))
             break;
         if (lane == 0)
             mbar_arrive_expect_tx(&c.bar.q_full[qb], (uint32_t)(it.g.nq * C::kHalves) * q_box_bytes);
@@ -306,6 +321,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             tma_load_3d(q_smem + (qb * kQTiles + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
                         h * 64, it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
         }
+        q_loads = n + 1;
         const int* bt_row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, it.b);
         const int n_pages_valid = (it.kv_len + P - 1) >> log2_p;
         for (int j = it.g.n_lo; ok && j <= it.g.n_hi; ++j) {
@@ -325,8 +341,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
                 for (int kind = 0; kind < 2; ++kind) {
                     const bool own = C::kSplitKV || kind == 0;  // this kind waits and posts its bytes
                     uint64_t* fb = (C::kSplitKV && kind) ? &c.bar.vfull[m] : &c.bar.full[m];
-                    if (own && !wait_bar((C::kSplitKV && kind) ? &c.bar.vempty[m] : &c.bar.empty[m], ph ^ 1,
-                                         c.abort_flag, p.err)) {
+                    if (own && !wait_bar((C::kSplitKV && kind) ? &c.bar.vempty[m] : &c.bar.empty[m], ph ^ 1, c)) {
                         ok = false;
                         break;
                     }
@@ -347,7 +362,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             } else {
                 for (int kind = 0; kind < 2; ++kind) {
                     const uint32_t s = ring_idx % kRingStages, ph = (ring_idx / kRingStages) & 1;
-                    if (!wait_bar(&rempty[s], ph ^ 1, c.abort_flag, p.err)) {
+                    if (!wait_bar(&rempty[s], ph ^ 1, c)) {
                         ok = false;
                         break;
                     }
@@ -367,7 +382,11 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         }
     }
     if (*c.abort_flag) {
-        // let the copies this warp started land before the CTA releases its memory
+        // let the copies this warp started land before the CTA releases its
+        // memory: the Q tiles of the last items (one buffer each), then K/V
+        const uint32_t q_first = q_loads > (uint32_t)C::kQBufs ? q_loads - C::kQBufs : 0;
+        for (uint32_t k = q_first; k < q_loads; ++k)
+            drain_wait(&c.bar.q_full[k % C::kQBufs], (k / C::kQBufs) & 1);
         if constexpr (FP8) {
             const uint32_t first = ring_idx > (uint32_t)kRingStages ? ring_idx - kRingStages : 0;
             for (uint32_t k = first; k < ring_idx; ++k)
@@ -440,7 +459,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     };
     // ring pair r % kPairs holds K (entry 2m) and V (entry 2m + 1) of the r-th tile
     auto wait_full = [&](uint32_t r) -> bool {
-        return wait_bar(&full[r % C::kPairs], (r / C::kPairs) & 1, c.abort_flag, p.err);
+        return wait_bar(&full[r % C::kPairs], (r / C::kPairs) & 1, c);
     };
     auto k_slot = [](uint32_t r) { return 2u * (r % C::kPairs); };
     auto v_slot = [](uint32_t r) { return 2u * (r % C::kPairs) + 1u; };
@@ -464,7 +483,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
         o.qb = n % C::kQBufs;
         // TMA (and converter) writes reach the MMA through the mbarrier alone:
         // no tcgen05 fence is needed after these waits
-        o.ok = wait_bar(FP8 ? &c.bar.q_conv[o.qb] : &c.bar.q_full[o.qb], (n / C::kQBufs) & 1, c.abort_flag, p.err);
+        o.ok = wait_bar(FP8 ? &c.bar.q_conv[o.qb] : &c.bar.q_full[o.qb], (n / C::kQBufs) & 1, c);
         o.first = ring_idx++;
         o.ok = o.ok && wait_full(o.first);
         return o;
@@ -484,9 +503,13 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     // The next item is opened while the current one's last kv tile finishes:
     // its S_0 right after the last P_0 V, its S_1 after the last P_1 V, the
     // same order as between two kv tiles of one item.
+    // failure-detection tests: a wait on a barrier nothing arrives on, which runs
+    // the wait limit out and sends the whole CTA down its abort path
+    if (p.inject_stall && !wait_bar(c.bar.never, 0, c))
+        ok = false;
     Open cur_item;
     ItemInfo info;
-    int w = take_item<C::kItemSlots>(p, c, 0, &ok, &info);
+    int w = ok ? take_item<C::kItemSlots>(p, c, 0, &ok, &info) : -1;
     if (w >= 0) {
         cur_item = open_item(info, 0);
         ok = cur_item.ok;
@@ -504,7 +527,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
             const bool last = j == n_hi;
             const uint32_t next = last ? 0u : ring_idx++;
             if ((FP8 || C::kSplitKV) &&
-                !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c.abort_flag, p.err)) {
+                !wait_bar(&c.bar.vfull[cur % C::kPairs], (cur / C::kPairs) & 1, c)) {
                 ok = false;
                 break;
             }
@@ -530,7 +553,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
                 if (!ok || t >= nq)
                     break;
                 for (int part = 0; part < C::kPParts; ++part) {
-                    if (!wait_bar(&c.bar.p_full[C::kPParts * t + part], p_cnt[t] & 1, c.abort_flag, p.err)) {
+                    if (!wait_bar(&c.bar.p_full[C::kPParts * t + part], p_cnt[t] & 1, c)) {
                         ok = false;
                         break;
                     }
@@ -632,7 +655,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         // query tile in it: a waiter that skipped phases could mistake a later
         // one for an earlier one); the row's Q was scaled by 2^k before its
         // conversion to f16, so its scores carry 2^k, taken out here
-        if (FP8 && !wait_bar(&c.bar.q_conv[n % C::kQBufs], (n / C::kQBufs) & 1, c.abort_flag, p.err)) {
+        if (FP8 && !wait_bar(&c.bar.q_conv[n % C::kQBufs], (n / C::kQBufs) & 1, c)) {
             ok = false;
             break;
         }
@@ -657,7 +680,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         float m_used = -INFINITY;
         float l = 0.f;
         for (int j = it.g.n_lo; j <= it.g.n_hi; ++j) {
-            if (!wait_bar(&c.bar.s_full[t], s_cnt & 1, c.abort_flag, p.err)) {
+            if (!wait_bar(&c.bar.s_full[t], s_cnt & 1, c)) {
                 ok = false;
                 break;
             }
@@ -792,7 +815,7 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
         if (!ok)
             break;
         // epilogue: out = bmm2_scale * O / (l + e^{sink - m})
-        if (!wait_bar(&c.bar.o_full[t], o_cnt & 1, c.abort_flag, p.err)) {
+        if (!wait_bar(&c.bar.o_full[t], o_cnt & 1, c)) {
             ok = false;
             break;
         }
@@ -951,7 +974,7 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
         // Q: thread ct takes row ct of each query tile: scale by 2^k into f16's
         // range, convert in place (same swizzled positions), post k
         const uint32_t qb = n % C::kQBufs, qph = (n / C::kQBufs) & 1;
-        if (!wait_bar(&c.bar.q_full[qb], qph, c.abort_flag, p.err))
+        if (!wait_bar(&c.bar.q_full[qb], qph, c))
             break;
         int8_t* qexp = reinterpret_cast<int8_t*>(c.base + C::kOffQExp) + (n & 1) * kQTiles * kQRows;
         for (int t = 0; t < it.g.nq; ++t) {
@@ -990,13 +1013,13 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
             const bool zero = j * kKvTile + ct >= it.kv_len;
             // the ring pair of this tile: K into entry 2m, V into 2m + 1
             const uint32_t m = r % C::kPairs;
-            if (!wait_bar(&c.bar.empty[m], ((r / C::kPairs) & 1) ^ 1, c.abort_flag, p.err)) {
+            if (!wait_bar(&c.bar.empty[m], ((r / C::kPairs) & 1) ^ 1, c)) {
                 ok = false;
                 break;
             }
             for (int kind = 0; kind < 2; ++kind) {
                 const uint32_t s8 = r8 % C::kF8Stages;
-                if (!wait_bar(&c.bar.f8full[s8], (r8 / C::kF8Stages) & 1, c.abort_flag, p.err)) {
+                if (!wait_bar(&c.bar.f8full[s8], (r8 / C::kF8Stages) & 1, c)) {
                     ok = false;
                     break;
                 }
@@ -1060,8 +1083,11 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
     c.bar.drain = c.bar.o_full + kQTiles;
     c.bar.it_full = c.bar.drain + 1;
     c.bar.it_empty = c.bar.it_full + C::kItemSlots;
+    c.bar.never = c.bar.it_empty + C::kItemSlots;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + C::kOffMisc);
     c.abort_flag = reinterpret_cast<volatile int*>(base + C::kOffMisc + 4);
+    c.err = p.err;
+    c.wait_limit_ns = p.wait_limit_ns;
     c.item_slot = reinterpret_cast<volatile int*>(base + C::kOffMisc + 16);
     const int warp = threadIdx.x >> 5;
 
@@ -1091,6 +1117,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
         for (int s = 0; s < C::kItemSlots; ++s) {
             mbar_init(&c.bar.it_full[s], 1);
             mbar_init(&c.bar.it_empty[s], C::kItemConsumerWarps);
+        mbar_init(c.bar.never, 1);
         }
         *c.abort_flag = 0;
         fence_mbar_init();

@@ -26,6 +26,8 @@ std::atomic<int> g_path{B2PA_PATH_AUTO};
 std::atomic<int> g_debug{0};
 std::atomic<void*> g_ev_start{nullptr};
 std::atomic<void*> g_ev_stop{nullptr};
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<int> g_inject_stall{0};
 
 int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int status, const char* fmt, ...)
@@ -489,6 +491,8 @@ int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, s
     ap->bmm2 = bmm2_scale;
     ap->bmm1_dev = bmm1_dev;
     ap->bmm2_dev = bmm2_dev;
+    ap->wait_limit_ns = g_wait_limit_ns.load();
+    ap->inject_stall = g_inject_stall.load();
     return B2PA_OK;
 }
 
@@ -1154,6 +1158,18 @@ int b2pa_set_timing_events(void* start_event, void* stop_event)
     const bool on = start_event != nullptr && stop_event != nullptr;
     g_ev_start.store(on ? start_event : nullptr);
     g_ev_stop.store(on ? stop_event : nullptr);
+    return B2PA_OK;
+}
+
+int b2pa_set_wait_limit_ns(uint64_t limit_ns)
+{
+    g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : (unsigned long long)limit_ns);
+    return B2PA_OK;
+}
+
+int b2pa_debug_inject_stall(int32_t on)
+{
+    g_inject_stall.store(on ? 1 : 0);
     return B2PA_OK;
 }
 

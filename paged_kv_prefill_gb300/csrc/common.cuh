@@ -17,7 +17,7 @@ constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the 
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 5 words per request in shared memory
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: a pipeline wait that exceeds this gives up
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: default pipeline wait limit; drains always use it
 
 // Where request b's query rows start: cum_q[b], or b * q_per_req for a decode
 // batch, whose requests all have q_per_req query tokens (cum_q null).
@@ -184,6 +184,8 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     int part_slots;      // chunks per row in the partial buffers
     float* part_o;       // [(token * H + head) * part_slots + chunk][D] unnormalised O (f32)
     float* part_ml;      // [(token * H + head) * part_slots + chunk][2] running maximum (log2 units) and sum
+    unsigned long long wait_limit_ns;  // pipeline waits give up after this long (B2PA_DEV_TIMEOUT)
+    int inject_stall;                  // failure-detection tests: one wait that nothing completes
     long long bt_stride;
     long long out_stride_tok;
     long long out_stride_head;

@@ -512,3 +512,42 @@ def test_stress_back_to_back_calls(cuda_lib, which):
     assert cuda_lib.device_status() == 0
     rows = _sample_rows(inp, 300, seed=5)
     _compare(out, inp, rows=rows)
+
+
+# ----------------------------------------------------------------- failure detection
+
+@pytest.mark.parametrize("variant", ["bf16_d128", "bf16_d64_window", "fp8", "decode_split"])
+def test_wait_timeout_returns_error_and_recovers(cuda_lib, variant):
+    """A pipeline wait that runs out: with the stall injected, each CTA's MMA
+    warp waits on a barrier that nothing arrives on, the 2 ms wait limit runs
+    out, and the CTA drains its copies and MMAs and exits; the call reports
+    B2PA_DEV_TIMEOUT without a GPU fault.  The same context then computes the
+    batch correctly with the stall off and the default limit."""
+    if variant == "decode_split":
+        inp = workload.build([1] * 4, [20000, 9000, 31000, 700], 32, 8, 128, 32, "HND", seed=43)
+    else:
+        D, W, kvd = {"bf16_d128": (128, -1, "bf16"), "bf16_d64_window": (64, 127, "bf16"),
+                     "fp8": (128, -1, "fp8_e4m3")}[variant]
+        inp = workload.build([200, 130], [900, 130], 8, 2, D, 32, "HND", kv_dtype=kvd, window_left=W, seed=41)
+
+    def call():
+        if variant == "decode_split":
+            d = _to_dev(inp)
+            out = torch.full_like(d["q"], float("nan"))
+            cuda_lib.batch_decode(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                  inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, -1, out, "HND", None,
+                                  q_len_per_req=1)
+            return out, cuda_lib.device_status()
+        return _run(cuda_lib, inp, "tcgen05")
+
+    cuda_lib.set_wait_limit_ns(2_000_000)
+    cuda_lib.debug_inject_stall(True)
+    try:
+        _, bits = call()
+    finally:
+        cuda_lib.debug_inject_stall(False)
+        cuda_lib.set_wait_limit_ns(0)
+    assert bits & cuda_lib.DEV_TIMEOUT
+    out, bits = call()
+    assert bits == 0
+    _compare(out, inp)
