@@ -392,7 +392,8 @@ int oracle_attention(const uint16_t* q, int64_t q_stride_tok, int64_t q_stride_h
  * cum_q[b] >= 0 or cum_q[b+1] <= num_tokens are not emitted.
  *
  * Order: by min(cost, cost_cap) descending; ties keep the enumeration order
- * (b ascending, then kv head, then it).  items_out gets 4 ints per item:
+ * (b ascending, then it, then kv head: the kv heads of one query item share
+ * its cost and sit side by side).  items_out gets 4 ints per item:
  * b, kv head, it, cost.  Returns the number of items (or -1 if more than
  * cap would be written).
  */
@@ -416,8 +417,8 @@ int oracle_worklist(const int32_t* cum_q, const int32_t* seq_lens, int B, int nu
             continue;
         int64_t prefix = kv_len - q_len;
         int64_t n_items = (q_len + per_item - 1) / per_item;
-        for (int hk = 0; hk < num_kv_heads; ++hk) {
-            for (int64_t it = 0; it < n_items; ++it) {
+        for (int64_t it = 0; it < n_items; ++it) {
+            for (int hk = 0; hk < num_kv_heads; ++hk) {
                 int64_t i0 = it * per_item;
                 int64_t i1 = i0 + per_item - 1;
                 if (i1 > q_len - 1)

@@ -383,8 +383,8 @@ def _brute_items(inp, rows_per_tile, nqt, bn):
         kl = int(inp.seq_lens[b])
         if ql == 0:
             continue
-        for hk in range(inp.num_kv_heads):
-            for it in range((ql + per - 1) // per):
+        for it in range((ql + per - 1) // per):
+            for hk in range(inp.num_kv_heads):
                 tiles, qtiles = set(), set()
                 for i in range(it * per, min(ql, (it + 1) * per)):
                     pos = kl - ql + i
