@@ -16,7 +16,7 @@ constexpr int kQTiles = 2;        // query tiles per work item (they share every
 constexpr int kCostCap = 1023;    // scheduler buckets: costs >= this share the top bucket
 constexpr int kSchedBuckets = kCostCap + 1;
 constexpr int kSchedThreads = 1024;
-constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 5 words per request in shared memory
+constexpr int kSchedMaxBatch = 4096;   // scheduler keeps 3 words per request in shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: default pipeline wait limit; drains always use it
 
 // Where request b's query rows start: cum_q[b], or b * q_per_req for a decode
