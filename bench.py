@@ -9,8 +9,8 @@ workload.config(2) with seed 1236.
 Metric: effective causal TFLOP/s = 4 * head_dim * num_heads * (visible (query,
 key) pairs) / time, with the fraction of the measured dense-bf16 tensor peak.
 
-One "step" = one b2pa_context_attention call over the whole batch (scheduler
-+ attention kernel).  Inputs are resident in HBM; L2 is flushed (a 512 MiB
+One "step" = one b2pa_context_attention call over the whole batch (one
+attention kernel, which also sorts its work items).  Inputs are resident in HBM; L2 is flushed (a 512 MiB
 write) before every timed step, outside the timed events.  Prints one JSON
 line on rank 0.
 
@@ -308,7 +308,7 @@ def run_all_workloads(reps: int = 20):
 
 def run_decode_workloads(reps: int = 20):
     """One JSON line per decode batch (b2pa_batch_decode): median time of the
-    whole call (scheduler, attention over kv chunks, combine) after a 512 MiB L2
+    whole call (attention over kv chunks, then the combine) after a 512 MiB L2
     flush, with algorithmic GB/s against the copy peak; decode streams the KV
     cache once, so HBM bandwidth is its roof."""
     import paged_kv_prefill_gb300 as b2pa
@@ -600,7 +600,7 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": Ke, "pipeline": "copies in / call / copies out on three streams, two device buffers"},
-            "gpu_launches": 2 * K,
+            "gpu_launches": K,
             "clocks": clocks,
             "wall_s_timed_region": wall,
         }

@@ -141,6 +141,12 @@ typedef struct {
  *
  * No host synchronisation.  Allocates (cudaMalloc) only when this stream's
  * workspace must grow; once grown, the call can be captured in a CUDA graph.
+ * On the tensor-core path the call is one kernel launch: every CTA sorts the
+ * work items itself at its start, and the first CTA to claim the job writes
+ * the list that the CTAs share after their first item (the stream's
+ * workspace holds it, with four counter words that each launch leaves at
+ * zero).  Calls on one stream must not overlap on the GPU, which stream order
+ * guarantees.
  */
 B2PA_API int b2pa_context_attention(const b2pa_tensor* q, const b2pa_tensor* k_pool, const b2pa_tensor* v_pool,
                            const b2pa_tensor* block_tables, const b2pa_tensor* seq_lens,
@@ -255,7 +261,7 @@ B2PA_API int b2pa_context_attention_tensor_scales(const b2pa_tensor* q, const b2
  * first use; this entry point calls no cudaMalloc, cudaFree or other
  * allocating routine.
  *
- * Its scratch (error word, work counter and the scheduler's work list) is a
+ * Its scratch (error word, work-distribution words and the work list) is a
  * fixed array inside the library: 256 B + 65536 work items x 16 B = 1 MiB +
  * 256 B, held on every GPU that loads the library until the process exits.
  * A call whose bounds need more than 65536 work items (batch x kv heads x
@@ -287,13 +293,14 @@ B2PA_API int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_ten
                            uint32_t* dev_status, b2pa_stream_t stream);
 
 /*
- * b2pa_debug_worklist -- run only the scheduler of the tensor-core path and
- * copy its work list to the host (synchronises `stream`).
+ * b2pa_debug_worklist -- build the work list of the tensor-core path (with a
+ * kernel that runs the same sort as the attention kernel's start) and copy it
+ * to the host (synchronises `stream`).
  *
  * Items are 4 int32 each: request b, kv head, item index it, cost.  Item it
  * of request b covers query tokens [it * n_qtiles * rows_per_tile, ...) and
  * cost = (kv tiles its rows touch) * (non-empty query tiles), sorted by
- * min(cost, cost_cap) descending, ties in (b, kv head, it) order.
+ * min(cost, cost_cap) descending, ties in (b, it, kv head) order.
  * geometry_out (may be NULL) receives {rows_per_tile, n_qtiles, kv_tile,
  * cost_cap}.  host_items_out holds cap items; *n_out gets the count (which
  * may exceed cap: only the first cap are copied).  Arguments as for

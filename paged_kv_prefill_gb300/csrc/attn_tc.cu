@@ -54,6 +54,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "worklist.cuh"
 
 namespace b2pa {
 
@@ -99,12 +100,19 @@ struct TcCfg {
     // both parities (a row's exponent is read by the softmax while the next
     // item's Q is being converted)
     static constexpr int kOffQExp = kOffMisc + 64 + kItemSlots * kItemRecWords * 4;
+    // this CTA's first item (int4; x = -1: none), from its own copy of the work list
+    static constexpr int kOffFirst = (kOffMisc + 16 + kItemSlots * kItemRecWords * 4 + 15) / 16 * 16;
+    static_assert(kOffFirst % 16 == 0 && kOffFirst + 16 <= kOffQExp, "misc layout");
     static constexpr int kQExpBytes = FP8 ? 2 * kQTiles * kQRows : 0;
     static constexpr int kSmemBytes = kOffQExp + kQExpBytes + 1024;  // + slack to align the base to 1024
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(!FP8 || D == 128, "fp8 path is D = 128");
     static_assert(kOCol + kQTiles * D <= kTmemCols, "tmem");
     static_assert(kSmemBytes <= 232448, "shared memory");
+    // the work list is sorted in the K/V ring at the kernel's start
+    static_assert(worklist_smem_ints(kThreads / 32, kSchedBuckets, kSchedMaxBatch) * sizeof(int) <=
+                      (size_t)kStages * kKvTileBytes,
+                  "work-list scratch");
 };
 
 struct Bars {
@@ -177,6 +185,27 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity)
     }
 }
 
+// Wait (lane 0 of the producer alone) until the work list that another CTA
+// of this launch writes is complete; false if this CTA gave up (abort flag,
+// or the wait limit ran out: then it raises both).
+__device__ __forceinline__ bool wait_list_ready(const int* ready, const Ctx& c)
+{
+    if (ld_acquire_gpu(ready) != 0)
+        return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_gpu(ready) == 0) {
+        if (*c.abort_flag != 0)
+            return false;
+        if (global_ns() - t0 > c.wait_limit_ns) {
+            *c.abort_flag = 1;
+            atomicOr(c.err, (unsigned)B2PA_DEV_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+    return true;
+}
+
 struct ItemInfo {
     int b, kvh, q0, q_len, kv_len;
     ItemGeom g;
@@ -184,10 +213,9 @@ struct ItemInfo {
 };
 
 template <bool SPLIT>
-__device__ __forceinline__ ItemInfo read_item(const AttnParams& p, int w)
+__device__ __forceinline__ ItemInfo read_item(const AttnParams& p, const int4 it)
 {
     ItemInfo r;
-    const int4 it = p.items[w];
     r.b = it.x;
     r.kvh = it.y;
     const QStarts cq{p.cum_q, p.q_per_req};
@@ -260,6 +288,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
     uint32_t ring_idx = 0;
     uint32_t ring_kv[2] = {0, 0};  // 16-bit path: K and V tiles whose copies were started
     uint32_t q_loads = 0;          // items whose Q copies were started
+    bool list_ready = false;       // lane 0: the shared work list was seen complete
     bool ok = true;
     // scales passed as device tensors are checked here: if they are unusable,
     // no item is taken, so every role finishes without writing anything
@@ -273,12 +302,27 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
             break;
         volatile int* rec = c.item_slot + slot * kItemRecWords;
         if (lane == 0) {
-            int w = scales_ok ? atomicAdd(p.counter, 1) : -1;
-            if (w >= c.n_items)
-                w = -1;
+            // the first item from this CTA's own copy of the list, later ones in
+            // list order from gridDim.x on, once the shared list is written
+            int w = -1;
+            int4 item = *reinterpret_cast<const int4*>(c.base + C::kOffFirst);
+            if (scales_ok && n == 0) {
+                w = item.x >= 0 && (int)blockIdx.x < c.n_items ? (int)blockIdx.x : -1;
+            } else if (scales_ok) {
+                w = (int)gridDim.x + atomicAdd(p.counter, 1);
+                if (w >= c.n_items)
+                    w = -1;
+                if (w >= 0 && !list_ready) {
+                    list_ready = wait_list_ready(p.ready, c);
+                    if (!list_ready)
+                        w = -1;
+                }
+                if (w >= 0)
+                    item = p.items[w];
+            }
             rec[0] = w;
             if (w >= 0) {
-                const ItemInfo r = read_item<SPLIT>(p, w);
+                const ItemInfo r = read_item<SPLIT>(p, item);
                 rec[1] = r.b;
                 rec[2] = r.kvh;
                 rec[3] = r.q0;
@@ -1117,8 +1161,8 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
         for (int s = 0; s < C::kItemSlots; ++s) {
             mbar_init(&c.bar.it_full[s], 1);
             mbar_init(&c.bar.it_empty[s], C::kItemConsumerWarps);
-        mbar_init(c.bar.never, 1);
         }
+        mbar_init(c.bar.never, 1);
         *c.abort_flag = 0;
         fence_mbar_init();
     }
@@ -1152,9 +1196,27 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
     tc_fence_after();
     c.tmem = *tmem_holder;
 
-    // the work list and the counter are written by the scheduler kernel that precedes this one
+    // inputs may come from the kernel this launch follows (and the work
+    // distribution words from the previous launch)
     pdl_wait();
-    c.n_items = min(*p.count, p.cap);
+    {
+        // every CTA sorts the work itself, in the K/V ring before any copy
+        // lands there; the first to win the claim also writes the list
+        int claim = 1;
+        if (threadIdx.x == 0)
+            claim = atomicCAS(p.claim, 0, 1);
+        const WorklistResult wl =
+            build_worklist<C::kThreads / 32>(p.sched, reinterpret_cast<int*>(base + C::kOffRing), blockIdx.x, claim);
+        if (wl.emit && threadIdx.x == 0) {
+            __threadfence();
+            st_release_gpu(p.ready, 1);
+        }
+        c.n_items = wl.n_items;
+        if (threadIdx.x == 0)
+            *reinterpret_cast<int4*>(base + C::kOffFirst) = wl.want;
+        fence_proxy_async_smem();  // the ring's next writes come through the async proxy
+        __syncthreads();
+    }
 
     if constexpr (FP8) {
         // 512 threads launch with 128 registers each; the softmax warpgroups
@@ -1188,6 +1250,16 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) {
+        // the last CTA out leaves the work-distribution words at zero
+        __threadfence();
+        if (atomicAdd(p.done, 1) == (int)gridDim.x - 1) {
+            *p.counter = 0;
+            *p.claim = 0;
+            *p.ready = 0;
+            *p.done = 0;
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(c.tmem, C::kTmemCols);

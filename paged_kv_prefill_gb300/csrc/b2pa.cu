@@ -80,7 +80,9 @@ int device_info(int* dev_out, DevInfo* info)
 
 // ------------------------------------------------------------------ workspaces
 
-// Per (device, stream): [0] error word, [4] item count, [8] work counter, [256 ..) work items.
+// Per (device, stream): [0] error word, [4] item count, [8] work counter,
+// [12] list claim, [16] list ready, [20] CTAs done (the attention kernel's
+// work distribution; zero between launches), [256 ..) work items.
 struct Workspace {
     int dev;
     cudaStream_t stream;
@@ -451,7 +453,7 @@ int encode_o_map(CUtensorMap* m, const Problem& pr, bool* ok)
 int rows_per_tile_of(const Problem& pr) { return kQRows / (pr.H / pr.Hkv); }
 
 // Everything the tensor-core kernel takes: tensor maps, pointers, geometry and
-// scales; the work list and counters come from the scheduler's parameters.
+// scales; the work list and its counters come from the scheduler's parameters.
 int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, size_t cap, int window,
                      float bmm1_scale, float bmm2_scale, const float* bmm1_dev = nullptr,
                      const float* bmm2_dev = nullptr)
@@ -475,9 +477,13 @@ int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, s
     ap->bt_stride = pr.bt_stride;
     ap->out_stride_tok = pr.out_st_tok;
     ap->out_stride_head = pr.out_st_head;
+    ap->sched = sp;  // callers that change sp afterwards copy it again
     ap->items = sp.items;
-    ap->count = sp.count;
-    ap->counter = sp.counter;
+    uint8_t* hdr = reinterpret_cast<uint8_t*>(sp.err);  // the workspace header
+    ap->counter = reinterpret_cast<int*>(hdr + 8);
+    ap->claim = reinterpret_cast<int*>(hdr + 12);
+    ap->ready = reinterpret_cast<int*>(hdr + 16);
+    ap->done = reinterpret_cast<int*>(hdr + 20);
     ap->err = sp.err;
     ap->cap = (int)cap;
     ap->H = pr.H;
@@ -562,7 +568,6 @@ SchedParams make_sched(const Problem& pr, const Workspace& ws, int max_q_len, in
     sp.nbuckets = (int)(max_cost + 1 < kSchedBuckets ? (max_cost + 1 > 2 ? max_cost + 1 : 2) : kSchedBuckets);
     sp.items = reinterpret_cast<int4*>(ws.mem + kWsHeader);
     sp.count = reinterpret_cast<int*>(ws.mem + 4);
-    sp.counter = reinterpret_cast<int*>(ws.mem + 8);
     sp.err = reinterpret_cast<unsigned*>(ws.mem);
     return sp;
 }
@@ -667,9 +672,8 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
             ap.part_ml = reinterpret_cast<float*>(ws.mem + off_ml);
             ap.part_o = reinterpret_cast<float*>(ws.mem + off_o);
         }
-        cudaError_t e = launch_schedule(sp, stream);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "scheduler launch");
+        ap.sched = sp;
+        cudaError_t e;
         cudaEvent_t ev0 = static_cast<cudaEvent_t>(g_ev_start.load());
         cudaEvent_t ev1 = static_cast<cudaEvent_t>(g_ev_stop.load());
         const bool timed = ev0 != nullptr && ev1 != nullptr;
@@ -1216,10 +1220,10 @@ void b2pa_release(void)
 
 // ====================================================================== allocation-free entry point
 //
-// b2pa_context_attention_noalloc runs the same scheduler and tensor-core
-// attention kernels as b2pa_context_attention, but the scratch they need (the
-// error word, the work counter, the item count and the work list) lives in the
-// fixed array below instead of a cudaMalloc'd per-stream workspace.
+// b2pa_context_attention_noalloc runs the same tensor-core attention kernel
+// as b2pa_context_attention, but the scratch it needs (the error word, the
+// work-distribution words and the work list) lives in the fixed array below
+// instead of a cudaMalloc'd per-stream workspace.
 
 namespace {
 
@@ -1305,12 +1309,10 @@ int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_tensor* k_po
     AttnParams ap;
     if ((st = fill_attn_params(&ap, pr, sp, cap, window, bmm1_scale, bmm2_scale)))
         return st;
-    // the error word must start at zero (the scheduler resets the work counter itself)
+    // the error word must start at zero (the kernel leaves its work-distribution words at zero itself)
     cudaError_t e = cudaMemsetAsync(mem, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(error word)");
-    if ((e = launch_schedule(sp, stream)) != cudaSuccess)
-        return cuda_fail(e, "scheduler launch");
     if ((e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true)) != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");
     if (dev_status && (e = cudaMemcpyAsync(dev_status, mem, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream)) !=

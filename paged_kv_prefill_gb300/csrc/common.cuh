@@ -163,7 +163,6 @@ struct SchedParams {
     int* nsplit;              // split-KV: chunks per request (0 for a request without work), for the combine
     int4* items;
     int* count;
-    int* counter;             // work counter of the attention kernel, reset here
     unsigned* err;
 };
 
@@ -189,9 +188,17 @@ struct AttnParams {  // 128-byte aligned through its CUtensorMap members
     long long bt_stride;
     long long out_stride_tok;
     long long out_stride_head;
+    // Work distribution.  Every CTA builds the longest-first list itself
+    // (sched: its inputs) and starts with item blockIdx.x; the first CTA to
+    // win `claim` also writes the list to `items` and then sets `ready`; later
+    // items are taken in order from gridDim.x on through `counter`.  The last
+    // CTA to finish (`done`) sets all four words back to zero for the next launch.
+    SchedParams sched;
     const int4* items;
-    const int* count;
-    int* counter;        // next work item (atomicAdd); zero at launch
+    int* counter;
+    int* claim;
+    int* ready;
+    int* done;
     unsigned* err;
     int cap;
     int H, Hkv, G, rows_per_tile, page_size, num_pages;

@@ -1,253 +1,28 @@
 // sched_gather.cu -- the work-list scheduler of the tensor-core path and the
 // debug gather that exercises its paged K/V loads.
-#include <climits>
 #include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "worklist.cuh"
 
 namespace b2pa {
 
 // ---------------------------------------------------------------------------
-// Scheduler: one CTA of 1024 threads.
-//
-// The sort runs over units (request b, query item it): every kv head of a
-// unit has the same tile range and cost, so each unit is decoded once and
-// expands to Hkv consecutive items (b, 0 .. Hkv-1, it) of the list.
-// 1. Validate each request (load_request) and count its units:
-//    ceil(q_len / (rows_per_tile * kQTiles)), or, for split-KV (decode)
-//    batches, the number of kv chunks of its one query item (cut in chunks
-//    of split_tiles kv tiles; it = the chunk index there).
-// 2. Enumerate units in (b, it) order; cost = kv tiles x non-empty query
-//    tiles (item_geometry), bucket = min(cost, nbuckets - 1).
-// 3. Stable counting sort by bucket, descending: each warp owns a contiguous
-//    slice of the enumeration and counts per bucket with __match_any_sync,
-//    a warp-shuffle scan over the warps gives each warp's offset within a
-//    bucket, a block scan over the buckets (descending) gives their starts,
-//    and a second pass scatters each unit's Hkv items to Hkv * its rank.
-// The list is thus ordered by cost (descending), then b, it, kv head; it is
-// fully deterministic.  Writes items[0 .. n) and *count = n; sets
-// B2PA_DEV_BAD_REQUEST for rejected requests (their items are not emitted).
+// Scheduler kernel: one CTA of 1024 threads builds and writes the work list
+// (build_worklist), for b2pa_debug_worklist.  The attention kernel builds the
+// same list itself at its start.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
-    }
-    if (lane == 31)
-        scratch[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o)
-                s += y;
-        }
-        scratch[lane] = s;  // inclusive warp totals
-    }
-    __syncthreads();
-    const int before = warp > 0 ? scratch[warp - 1] : 0;
-    if (total)
-        *total = scratch[(blockDim.x >> 5) - 1];
-    const int r = before + x - v;
-    __syncthreads();
-    return r;
-}
-
 __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(const SchedParams p)
 {
-    // let the attention kernel start its prologue while the list is built
-    pdl_launch_dependents();
     extern __shared__ int sm[];
-    const int B = p.B;
-    const int nb = p.nbuckets;
-    const int Hkv = p.Hkv;
-    int* hist = sm;                                  // [32 warps][nb]
-    int* scratch = hist + 32 * nb;                   // 64
-    int* tot = scratch + 64;                         // [nb]
-    int* req_start = tot + nb;                       // [B + 1] first unit of each request
-    int* req_q = req_start + B + 1;                  // [B] q_len
-    int* req_kv = req_q + B;                         // [B] kv_len
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per_item = p.rows_per_tile * kQTiles;
-    if (tid == 0)
-        *p.counter = 0;
-
-    // 1. per-request unit counts, as a block-wide scan over contiguous chunks
-    const int chunk = (B + kSchedThreads - 1) / kSchedThreads;
-    const int b_begin = min(B, tid * chunk), b_end = min(B, b_begin + chunk);
-    int local = 0;
-    for (int b = b_begin; b < b_end; ++b) {
-        const RequestView r = load_request(QStarts{p.cum_q, p.q_per_req}, p.seq_lens, b, p.max_q_len, p.max_kv_len,
-                                           p.page_size, p.max_pages, p.num_tokens);
-        if (!r.ok)
-            atomicOr(p.err, (unsigned)B2PA_DEV_BAD_REQUEST);
-        int n_it = (r.ok && r.q_len > 0) ? (r.q_len + per_item - 1) / per_item : 0;  // units (per kv head: items)
-        if (p.split_tiles > 0) {
-            // one query item per kv head (the host makes q_len fit), cut in kv chunks
-            const int ns = n_it > 0 ? split_count(item_geometry(r.q_len, r.kv_len, 0, p.rows_per_tile, p.window),
-                                                  p.split_tiles)
-                                    : 0;
-            p.nsplit[b] = ns;
-            n_it = ns;
-        }
-        req_start[b] = n_it;  // count for now
-        req_q[b] = r.q_len;
-        req_kv[b] = r.kv_len;
-        local += n_it;
-        if (p.debug) {
-            if (p.cum_kv != nullptr && r.ok && p.cum_kv[b + 1] - p.cum_kv[b] != r.kv_len)
-                atomicOr(p.err, (unsigned)B2PA_DEV_BAD_CUM_KV);
-            if (r.ok) {
-                const int pages = (r.kv_len + p.page_size - 1) / p.page_size;
-                const int* row = page_row(p.block_tables, p.bt_stride, p.kv_indptr, b);
-                for (int col = 0; col < pages; ++col) {
-                    const int id = row[col];
-                    if (id < 0 || id >= p.num_pages)
-                        atomicOr(p.err, (unsigned)B2PA_DEV_BAD_PAGE);
-                }
-            }
-        }
-    }
-    for (int k = tid; k < 32 * nb; k += kSchedThreads)
-        hist[k] = 0;
-    int n_units = 0;
-    int run = block_exclusive_scan(local, scratch, &n_units);
-    for (int b = b_begin; b < b_end; ++b) {
-        const int n = req_start[b];
-        req_start[b] = run;
-        run += n;
-    }
-    const long long n_total = (long long)n_units * Hkv;
-    if (tid == 0) {
-        req_start[B] = n_units;
-        if (n_total > p.cap)
-            atomicOr(p.err, (unsigned)B2PA_DEV_OVERFLOW);
-    }
-    __syncthreads();
-
-    // unit u -> (b, it, cost, bucket)
-    auto decode = [&](int u, int4& unit, int& bucket) {
-        int lo = 0, hi = B - 1;  // last b with req_start[b] <= u
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (req_start[mid] <= u)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int b = lo;
-        const int it = u - req_start[b];  // split-KV: the chunk index (the query item is 0)
-        ItemGeom g = item_geometry(req_q[b], req_kv[b], p.split_tiles > 0 ? 0 : it, p.rows_per_tile, p.window);
-        if (p.split_tiles > 0)
-            split_range(&g, it, p.split_tiles);
-        const int cost = (g.n_hi - g.n_lo + 1) * g.nq;
-        unit = make_int4(b, 0, it, cost);
-        bucket = min(cost, nb - 1);
-    };
-
-    const int seg = (n_units + 31) / 32;
-    const int s_begin = min(n_units, warp * seg), s_end = min(n_units, s_begin + seg);
-    int* my_hist = hist + warp * nb;
-
-    // 2. per-warp bucket counts.  The first kKeep rounds of 32 units stay in
-    // registers for the scatter; later rounds are decoded again there.
-    constexpr int kKeep = 2;
-    int4 kept_unit[kKeep];
-    int kept_bucket[kKeep];
-    auto count_round = [&](int bucket) {
-        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
-        if (bucket >= 0 && lane == __ffs(grp) - 1)
-            my_hist[bucket] += __popc(grp);
-        __syncwarp();
-    };
-#pragma unroll
-    for (int k = 0; k < kKeep; ++k) {
-        const int u = s_begin + 32 * k + lane;
-        kept_unit[k] = make_int4(0, 0, 0, 0);
-        kept_bucket[k] = -1;
-        if (u < s_end)
-            decode(u, kept_unit[k], kept_bucket[k]);
-        if (s_begin + 32 * k < s_end)  // warp-uniform
-            count_round(kept_bucket[k]);
-    }
-    for (int base = s_begin + 32 * kKeep; base < s_end; base += 32) {
-        const int u = base + lane;
-        int4 unit;
-        int bucket = -1;
-        if (u < s_end)
-            decode(u, unit, bucket);
-        count_round(bucket);
-    }
-    __syncthreads();
-
-    // 3. offsets: buckets in descending order, warps in ascending order.
-    // Within a bucket, the warps' counts are scanned by one warp (lane w holds
-    // warp w's count); warp u takes buckets u, u + 32, ...
-    for (int c = warp; c < nb; c += 32) {
-        const int v = hist[lane * nb + c];
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o)
-                x += y;
-        }
-        hist[lane * nb + c] = x - v;
-        if (lane == 31)
-            tot[c] = x;
-    }
-    __syncthreads();
-    // exclusive scan over buckets from the top: thread t takes bucket nb - 1 - t
-    // (nb <= kSchedBuckets == kSchedThreads); tot then holds each bucket's start
-    const int start = block_exclusive_scan(tid < nb ? tot[nb - 1 - tid] : 0, scratch, nullptr);
-    if (tid < nb)
-        tot[nb - 1 - tid] = start;
-    __syncthreads();
-
-    // 4. scatter, in the same order as the counts: a unit of rank r fills
-    // items Hkv * r .. Hkv * r + Hkv - 1, one per kv head
-    auto scatter_round = [&](const int4& unit, int bucket) {
-        const unsigned grp = __match_any_sync(0xffffffffu, bucket);
-        const unsigned lower = grp & ((1u << lane) - 1u);
-        if (bucket >= 0) {
-            const long long pos = (long long)(tot[bucket] + my_hist[bucket] + __popc(lower)) * Hkv;
-            for (int h = 0; h < Hkv; ++h)
-                if (pos + h < p.cap)
-                    p.items[pos + h] = make_int4(unit.x, h, unit.z, unit.w);
-        }
-        __syncwarp();
-        if (bucket >= 0 && lane == __ffs(grp) - 1)
-            my_hist[bucket] += __popc(grp);
-        __syncwarp();
-    };
-#pragma unroll
-    for (int k = 0; k < kKeep; ++k)
-        if (s_begin + 32 * k < s_end)  // warp-uniform
-            scatter_round(kept_unit[k], kept_bucket[k]);
-    for (int base = s_begin + 32 * kKeep; base < s_end; base += 32) {
-        const int u = base + lane;
-        int4 unit = make_int4(0, 0, 0, 0);
-        int bucket = -1;
-        if (u < s_end)
-            decode(u, unit, bucket);
-        scatter_round(unit, bucket);
-    }
-    if (tid == 0)
-        *p.count = (int)min(n_total, (long long)INT_MAX);
+    build_worklist<kSchedThreads / 32>(p, sm, -1, 0);
 }
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
 {
     const size_t nb = (size_t)p.nbuckets;
-    const size_t smem = sizeof(int) * (32 * nb + 64 + nb + 3 * (size_t)p.B + 1);
+    const size_t smem = sizeof(int) * worklist_smem_ints(kSchedThreads / 32, (int)nb, p.B);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -259,7 +34,7 @@ cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream)
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     std::call_once(attr_once[dev], [&] {
-        const size_t most = sizeof(int) * (32 * (size_t)kSchedBuckets + 64 + kSchedBuckets + 3 * (size_t)kSchedMaxBatch + 1);
+        const size_t most = sizeof(int) * worklist_smem_ints(kSchedThreads / 32, kSchedBuckets, kSchedMaxBatch);
         attr_err[dev] = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     });
     if (attr_err[dev] != cudaSuccess)
