@@ -75,7 +75,12 @@ struct TcCfg {
     static constexpr int kStages = D == 128 ? 4 : 8;                // 16-bit ring entries
     static constexpr int kPairs = kStages / 2;                      // tiles in the ring
     static constexpr bool kSplitKV = D == 128 && !FP8;              // K and V released separately
-    static constexpr int kF8Stages = FP8 ? 2 : 0;                   // e4m3 staging ring
+    // Query tiles held per Q buffer.  A split-KV (decode) batch on the e4m3 path
+    // runs with one query tile per item (the host splits only such batches), and
+    // the room goes to a deeper e4m3 staging ring: there the K/V stream, not the
+    // tensor core, sets the rate, and two tiles in flight hide more of HBM's latency.
+    static constexpr int kQTilesAlloc = FP8 && SPLIT ? 1 : kQTiles;
+    static constexpr int kF8Stages = FP8 ? (SPLIT ? 4 : 2) : 0;     // e4m3 staging ring
     static constexpr int kF8TileBytes = kKvTile * D;  // e4m3 tile: 128 rows of D bytes
     static constexpr int kThreads = FP8 ? 512 : 384;
     static constexpr int kItemSlots = 4;
@@ -83,7 +88,7 @@ struct TcCfg {
     static constexpr int kTmemCols = 512;
     static constexpr int kOCol = 2 * kKvTile;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffRing = kOffQ + kQBufs * kQTiles * kQTileBytes;
+    static constexpr int kOffRing = kOffQ + kQBufs * kQTilesAlloc * kQTileBytes;
     static constexpr int kOffF8 = kOffRing + kStages * kKvTileBytes;
     // output staging (16-bit KV paths; the e4m3 path has no room): per softmax
     // warp, 32 rows x 64 columns of bf16, so that the output leaves in whole
@@ -362,7 +367,7 @@ __device__ void producer_role(const AttnParams& p, const Ctx& c)
         __syncwarp();
         if (lane < it.g.nq * C::kHalves) {
             const int t = lane / C::kHalves, h = lane % C::kHalves;
-            tma_load_3d(q_smem + (qb * kQTiles + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
+            tma_load_3d(q_smem + (qb * C::kQTilesAlloc + t) * C::kQTileBytes + h * C::kHalfBytes, &p.tm_q, &c.bar.q_full[qb],
                         h * 64, it.kvh * p.G, it.q0 + it.g.tok0 + t * p.rows_per_tile);
         }
         q_loads = n + 1;
@@ -479,7 +484,7 @@ __device__ void mma_role(const AttnParams& p, const Ctx& c)
     constexpr uint32_t kHalfW = C::kHalfBytes >> 4;
 
     auto issue_s = [&](uint32_t qb, int t, uint32_t slot) {
-        const uint32_t a0 = q_lo + (qb * kQTiles + t) * kQTileW;
+        const uint32_t a0 = q_lo + (qb * C::kQTilesAlloc + t) * kQTileW;
         const uint32_t b0 = k_lo + slot * kStageW;
         const uint32_t d = c.tmem + (uint32_t)(t * kKvTile);
 #pragma unroll
@@ -1022,7 +1027,7 @@ __device__ void convert_role(const AttnParams& p, const Ctx& c)
             break;
         int8_t* qexp = reinterpret_cast<int8_t*>(c.base + C::kOffQExp) + (n & 1) * kQTiles * kQRows;
         for (int t = 0; t < it.g.nq; ++t) {
-            uint8_t* qrow = c.base + C::kOffQ + (qb * kQTiles + t) * C::kQTileBytes + ct * 128;
+            uint8_t* qrow = c.base + C::kOffQ + (qb * C::kQTilesAlloc + t) * C::kQTileBytes + ct * 128;
             uint32_t mx = 0;  // largest magnitude of the row, as bf16 bits
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -1183,7 +1188,7 @@ __global__ void __launch_bounds__(TcCfg<D, FP8, SPLIT>::kThreads, 1) attention_t
         const int pad = C::kHalfBytes - used;
         if (pad > 0) {
             const int n16 = pad / 16;
-            for (int k = threadIdx.x; k < C::kQBufs * kQTiles * C::kHalves * n16; k += blockDim.x) {
+            for (int k = threadIdx.x; k < C::kQBufs * C::kQTilesAlloc * C::kHalves * n16; k += blockDim.x) {
                 const int blk = k / n16, q = k % n16;
                 *reinterpret_cast<uint4*>(base + C::kOffQ + blk * C::kHalfBytes + used + q * 16) =
                     make_uint4(0u, 0u, 0u, 0u);

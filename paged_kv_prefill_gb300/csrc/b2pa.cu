@@ -586,7 +586,8 @@ SplitPlan plan_split(const Problem& pr, int max_kv_len, int sms)
 {
     SplitPlan sp;
     const int G = pr.H / pr.Hkv;
-    const int per_item = (kQRows / G) * kQTiles;
+    // the e4m3 split kernel holds one query tile per item
+    const int per_item = (kQRows / G) * (pr.fp8 ? 1 : kQTiles);
     if (pr.q_per_req <= 0 || pr.q_per_req > per_item)
         return sp;  // several query items per request: no split (as a context batch)
     const long long tiles = (max_kv_len + kKvTile - 1) / kKvTile;
