@@ -7,10 +7,10 @@
 // e4m3 pool gets x / scale (one IEEE binary32 division) converted by
 // cvt.rn.satfinite: round to nearest even, saturating at +-448.
 //
-// HBM-bound: one thread moves one 8-element chunk (16 bytes in; 16 bytes out
-// for bf16, 8 for e4m3) of a (token, kv head) row of K and the same chunk of
-// V; consecutive threads take consecutive chunks of a row, so a warp reads and
-// writes whole rows.  Grid-stride over T * Hkv * D / 8 chunks.
+// HBM-bound: a thread moves 8-element chunks (16 bytes in; 16 bytes out for
+// bf16, 8 for e4m3) of (token, kv head) rows of K and the same chunks of V;
+// consecutive threads take consecutive chunks of a row, so a warp reads and
+// writes whole rows.  One grid covers all T * Hkv * D / 8 chunks.
 #include "../../include/b2pa.h"
 #include "append.cuh"
 
@@ -38,49 +38,82 @@ __device__ __forceinline__ uint2 quantise8(uint4 x, float scale)
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
+// Each thread moves kUnroll chunks, kUnroll * 256 apart, issuing every load
+// before its first store so that the copies overlap (one chunk per thread for
+// an e4m3 pool, whose 16 divisions per chunk are better spread over more
+// threads).  Idx: 32-bit index math when the chunk count allows it, else 64-bit.
+constexpr int kAppendThreads = 256;
 template <bool FP8>
-__global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p)
+constexpr int append_unroll() { return FP8 ? 1 : 4; }
+
+template <bool FP8, typename Idx>
+__global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const AppendParams p, const Idx total)
 {
-    const int chunks = p.D >> 3;
-    const long long total = (long long)p.T * p.Hkv * chunks;
+    constexpr int kUnroll = append_unroll<FP8>();
+    const Idx chunks = (Idx)(p.D >> 3);
     const long long slots = (long long)p.num_pages * p.page_size;
-    const long long step = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += step) {
-        const int c = (int)(i % chunks);
-        const long long r = i / chunks;
-        const int h = (int)(r % p.Hkv);
-        const long long n = r / p.Hkv;
-        const int loc = p.cache_loc[n];
-        if (loc < 0 || (long long)loc >= slots) {
-            if (h == 0 && c == 0)
+    const Idx base = (Idx)blockIdx.x * (kAppendThreads * kUnroll) + (Idx)threadIdx.x;
+    uint4 kx[kUnroll], vx[kUnroll];
+    int loc[kUnroll], h[kUnroll], c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const Idx i = base + (Idx)u * kAppendThreads;
+        loc[u] = -1;
+        if (i < total) {
+            c[u] = (int)(i % chunks);
+            const Idx r = i / chunks;
+            h[u] = (int)(r % (Idx)p.Hkv);
+            const Idx n = r / (Idx)p.Hkv;
+            loc[u] = p.cache_loc[n];
+            const long long src = (long long)n * p.new_st_tok + (long long)h[u] * p.new_st_head + 8 * c[u];
+            kx[u] = *reinterpret_cast<const uint4*>(p.k_new + src);
+            vx[u] = *reinterpret_cast<const uint4*>(p.v_new + src);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const Idx i = base + (Idx)u * kAppendThreads;
+        if (i >= total)
+            continue;
+        if (loc[u] < 0 || (long long)loc[u] >= slots) {
+            if (h[u] == 0 && c[u] == 0)
                 atomicOr(p.err, (unsigned)B2PA_DEV_BAD_SLOT);
             continue;
         }
-        const long long page = loc / p.page_size, slot = loc - page * p.page_size;
-        const long long src = n * p.new_st_tok + (long long)h * p.new_st_head + 8 * c;
-        const uint4 kx = *reinterpret_cast<const uint4*>(p.k_new + src);
-        const uint4 vx = *reinterpret_cast<const uint4*>(p.v_new + src);
-        const long long dk = page * p.k_st[0] + h * p.k_st[1] + slot * p.k_st[2] + 8 * c;
-        const long long dv = page * p.v_st[0] + h * p.v_st[1] + slot * p.v_st[2] + 8 * c;
+        const long long page = loc[u] / p.page_size, slot = loc[u] - page * p.page_size;
+        const long long dk = page * p.k_st[0] + h[u] * p.k_st[1] + slot * p.k_st[2] + 8 * c[u];
+        const long long dv = page * p.v_st[0] + h[u] * p.v_st[1] + slot * p.v_st[2] + 8 * c[u];
         if constexpr (FP8) {
-            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_pool) + dk) = quantise8(kx, p.k_scale);
-            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_pool) + dv) = quantise8(vx, p.v_scale);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_pool) + dk) = quantise8(kx[u], p.k_scale);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_pool) + dv) = quantise8(vx[u], p.v_scale);
         } else {
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_pool) + dk) = kx;
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_pool) + dv) = vx;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_pool) + dk) = kx[u];
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_pool) + dv) = vx[u];
         }
     }
 }
 
-cudaError_t launch_append(const AppendParams& p, bool fp8, int grid, cudaStream_t stream)
+template <bool FP8>
+static cudaError_t launch_typed(const AppendParams& p, long long total, cudaStream_t stream)
 {
-    if (p.T == 0 || grid <= 0)
-        return cudaSuccess;
-    if (fp8)
-        append_kv_kernel<true><<<grid, 256, 0, stream>>>(p);
+    const long long per_block = (long long)kAppendThreads * append_unroll<FP8>();
+    const long long blocks = (total + per_block - 1) / per_block;
+    if (blocks > 0x7FFFFFFFLL)
+        return cudaErrorInvalidConfiguration;
+    if (total <= 0x7FFFFFFFLL - per_block)
+        append_kv_kernel<FP8, unsigned><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(p, (unsigned)total);
     else
-        append_kv_kernel<false><<<grid, 256, 0, stream>>>(p);
+        append_kv_kernel<FP8, unsigned long long><<<(unsigned)blocks, kAppendThreads, 0, stream>>>(
+            p, (unsigned long long)total);
     return cudaGetLastError();
+}
+
+cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream)
+{
+    const long long total = (long long)p.T * p.Hkv * (p.D >> 3);
+    if (total == 0)
+        return cudaSuccess;
+    return fp8 ? launch_typed<true>(p, total, stream) : launch_typed<false>(p, total, stream);
 }
 
 }  // namespace b2pa

@@ -20,7 +20,7 @@ struct AppendParams {
     unsigned* err;
 };
 
-// grid: blocks of 256 threads; each thread moves 8 elements of K and of V per step
-cudaError_t launch_append(const AppendParams& p, bool fp8, int grid, cudaStream_t stream);
+// one launch over every chunk; each thread moves 8 elements of K and of V per chunk
+cudaError_t launch_append(const AppendParams& p, bool fp8, cudaStream_t stream);
 
 }  // namespace b2pa

@@ -1082,11 +1082,7 @@ int b2pa_append_kv(const b2pa_tensor* k_new, const b2pa_tensor* v_new, const b2p
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
     ap.err = reinterpret_cast<unsigned*>(ws.mem);
-    // enough 256-thread blocks for every chunk, at most 8 per SM (grid-stride beyond)
-    const long long chunks = T * (long long)pr.Hkv * (pr.D / 8);
-    const long long want = (chunks + 255) / 256;
-    const int grid = (int)(want < 8LL * di.sms ? want : 8LL * di.sms);
-    cudaError_t e = launch_append(ap, pr.fp8, grid, stream);
+    cudaError_t e = launch_append(ap, pr.fp8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "append launch");
     return B2PA_OK;
