@@ -52,6 +52,7 @@ DECODE_CASES = [
     (16, 4, 32768, 32, 8, 128, 32, "HND", "fp8_e4m3", -1, False),  # e4m3 cache
     (8, 2, 20000, 64, 8, 64, 16, "HND", "bf16", 127, True),       # D = 64, sliding window + sinks
     (8, 3, 9000, 12, 4, 128, 64, "NHD", "bf16", -1, False),       # G = 3 (rows 126 of 128), q_len 3
+    (4, 40, 9000, 32, 8, 128, 32, "HND", "fp8_e4m3", -1, True),   # e4m3, more rows than one tile: not split
 ]
 
 

@@ -491,6 +491,33 @@ def test_invalid_arguments_rejected_on_host(cuda_lib):
                                    1.0, d["cum_q"], None, -1, None, "HND")
 
 
+def test_two_streams_concurrently(cuda_lib):
+    """Calls on two streams at once: each stream has its own workspace, so the
+    work-distribution words and work lists of the two launches are separate;
+    both results must match the oracle (and the single-stream result bit for
+    bit), round after round."""
+    a = workload.build([300, 1, 700, 64], [900, 40, 700, 2000], 32, 8, 128, 32, "HND", seed=71, with_sinks=True)
+    b = workload.build([129, 1000], [129, 3000], 16, 2, 64, 16, "NHD", seed=72, window_left=200)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for inp in (a, b):
+        d = _to_dev(inp)
+        outs.append((inp, d, torch.full_like(d["q"], float("nan"))))
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for (inp, d, out), st in zip(outs, (s1, s2)):
+            cuda_lib.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                       inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"],
+                                       d["cum_kv"], inp.window_left, out, inp.layout, d["sinks"], stream=st)
+    assert cuda_lib.device_status(s1) == 0 and cuda_lib.device_status(s2) == 0
+    torch.cuda.synchronize()
+    for inp, d, out in outs:
+        _compare(out, inp)
+        single, bits = _run(cuda_lib, inp)
+        assert bits == 0
+        assert torch.equal(single.view(torch.int16), out.view(torch.int16))
+
+
 @pytest.mark.parametrize("which", ["ragged_lone_tiles", "cfg2", "cfg5"])
 def test_stress_back_to_back_calls(cuda_lib, which):
     """Hundreds of calls in a row (the pattern a timed benchmark produces): no
