@@ -680,7 +680,9 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
         const bool timed = ev0 != nullptr && ev1 != nullptr;
         if (timed && (e = cudaEventRecord(ev0, stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
-        e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, !timed);
+        // launched as every call launches it; with the events around it the
+        // kernel follows the start event, not an earlier kernel
+        e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true);
         if (e != cudaSuccess)
             return cuda_fail(e, "attention kernel launch");
         if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
