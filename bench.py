@@ -405,6 +405,36 @@ def new_token_slots(inp):
     return torch.cat(loc).to(torch.int32)
 
 
+def run_profile_workload(name: str, warmup: int, steps: int):
+    """For ncu: W warm-up calls then K calls of another named workload (the
+    sliding-window layer or a decode batch), each after an L2 flush; prints no
+    measurement."""
+    import paged_kv_prefill_gb300 as b2pa
+    from paged_kv_prefill_gb300 import build as b2pa_build
+
+    b2pa_build.build()
+    b2pa.load()
+    dev = torch.device("cuda", 0)
+    decode = name == "decode_q1"
+    inp = workload.decode_config(1) if decode else workload.config(4)
+    d = {n: getattr(inp, n).to(dev) for n in ("q", "k_pool", "v_pool", "block_tables", "seq_lens", "cum_q", "cum_kv")}
+    sinks = None if inp.sinks is None else inp.sinks.to(dev)
+    out = torch.empty_like(d["q"])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    for i in range(warmup + steps):
+        flush.fill_(i)
+        if decode:
+            b2pa.batch_decode(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"], inp.max_kv_len,
+                              inp.bmm1_scale, inp.bmm2_scale, inp.window_left, out, inp.layout, sinks,
+                              q_len_per_req=1)
+        else:
+            b2pa.context_attention(d["q"], (d["k_pool"], d["v_pool"]), d["block_tables"], d["seq_lens"],
+                                   inp.max_q_len, inp.max_kv_len, inp.bmm1_scale, inp.bmm2_scale, d["cum_q"],
+                                   d["cum_kv"], inp.window_left, out, inp.layout, sinks)
+    torch.cuda.synchronize()
+    print(f"profile run ({inp.name}): {warmup} + {steps} calls, device bits {b2pa.device_status()}", flush=True)
+
+
 def run_ours(args, world, rank, local):
     import paged_kv_prefill_gb300 as b2pa
     from paged_kv_prefill_gb300 import build as b2pa_build
@@ -678,6 +708,8 @@ def main():
                     help="time only the decode batches (b2pa_batch_decode)")
     ap.add_argument("--profile", action="store_true",
                     help="only W + K calls of the workload (for ncu); prints no measurement")
+    ap.add_argument("--profile-workload", choices=["swa127", "decode_q1"],
+                    help="as --profile, for the sliding-window layer or the q_len_per_req 1 decode batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -689,6 +721,9 @@ def main():
         return
     if args.decode:
         run_decode_workloads()
+        return
+    if args.profile_workload:
+        run_profile_workload(args.profile_workload, args.warmup, args.steps)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":
