@@ -48,7 +48,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_tc_llama3_8b_prefill_traffic.json")
-KERNEL_SOURCES = ["attn_tc.cu", "common.cuh", "ptx.cuh", "worklist.cuh"]
+KERNEL_SOURCES = ["attn_tc.cu", "attn_common.cuh", "common.cuh", "ptx.cuh", "worklist.cuh"]
 
 
 # --------------------------------------------------------------------------- workload arithmetic

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libb2pa.so")
-SOURCES = ["b2pa.cu", "attn_tc.cu", "sched_gather.cu", "generic.cu", "append.cu", "decode.cu"]
+SOURCES = ["b2pa.cu", "attn_tc.cu", "attn_win.cu", "sched_gather.cu", "generic.cu", "append.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                 "--expt-relaxed-constexpr", "-I", os.path.join(os.path.dirname(HERE), "include")]

@@ -452,6 +452,23 @@ int encode_o_map(CUtensorMap* m, const Problem& pr, bool* ok)
 
 int rows_per_tile_of(const Problem& pr) { return kQRows / (pr.H / pr.Hkv); }
 
+// The one-window-tile kernel takes a tensor-core shape at head_dim 64 with a
+// 16-bit cache, a left window, no kv chunks and pages of at most 32 keys, when
+// every row of a work item (two query tiles) sees keys within one tile of
+// win_max_keys() keys that starts at a page boundary.
+bool win_eligible(const Problem& pr, int window, bool split)
+{
+    return !pr.fp8 && pr.D == 64 && window >= 0 && !split && pr.P <= 32 &&
+           2LL * rows_per_tile_of(pr) + window + pr.P - 1 <= win_max_keys();
+}
+
+cudaError_t launch_tc_kernel(const AttnParams& ap, const Problem& pr, int window, bool split, int sms,
+                             cudaStream_t stream)
+{
+    return win_eligible(pr, window, split) ? launch_attention_win(ap, sms, stream)
+                                           : launch_attention_tc(ap, pr.D, pr.fp8, sms, stream, true);
+}
+
 // Everything the tensor-core kernel takes: tensor maps, pointers, geometry and
 // scales; the work list and its counters come from the scheduler's parameters.
 int fill_attn_params(AttnParams* ap, const Problem& pr, const SchedParams& sp, size_t cap, int window,
@@ -682,7 +699,7 @@ int context_attention_impl(const b2pa_tensor* q, const b2pa_tensor* k_pool, cons
             return cuda_fail(e, "cudaEventRecord");
         // launched as every call launches it; with the events around it the
         // kernel follows the start event, not an earlier kernel
-        e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true);
+        e = launch_tc_kernel(ap, pr, window, split.split_tiles > 0, di.sms, stream);
         if (e != cudaSuccess)
             return cuda_fail(e, "attention kernel launch");
         if (timed && (e = cudaEventRecord(ev1, stream)) != cudaSuccess)
@@ -1312,7 +1329,7 @@ int b2pa_context_attention_noalloc(const b2pa_tensor* q, const b2pa_tensor* k_po
     cudaError_t e = cudaMemsetAsync(mem, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync(error word)");
-    if ((e = launch_attention_tc(ap, pr.D, pr.fp8, di.sms, stream, true)) != cudaSuccess)
+    if ((e = launch_tc_kernel(ap, pr, window, false, di.sms, stream)) != cudaSuccess)
         return cuda_fail(e, "attention kernel launch");
     if (dev_status && (e = cudaMemcpyAsync(dev_status, mem, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream)) !=
                           cudaSuccess)

@@ -265,6 +265,9 @@ struct CombineParams {
 // Host launchers (one translation unit each).
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 cudaError_t launch_attention_tc(const AttnParams& p, int head_dim, bool fp8, int grid, cudaStream_t stream, bool pdl);
+// the one-window-tile kernel for short left windows at head_dim 64 (attn_win.cu)
+cudaError_t launch_attention_win(const AttnParams& p, int grid, cudaStream_t stream);
+int win_max_keys();
 cudaError_t launch_gather(const GatherParams& p, bool fp8, int max_kv_len, cudaStream_t stream);
 cudaError_t launch_attention_generic(const GenericParams& p, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);

@@ -127,6 +127,10 @@ TC_CASES = [
     ([300, 7], [300, 600], 8, 2, 128, 64, "NHD", 77, True, "fp8_e4m3"),
     ([0, 40, 0, 10], [10, 100, 0, 10], 8, 2, 128, 32, "HND", -1, False, "bf16"),  # empty requests
     ([24, 24], [24, 24], 12, 4, 128, 32, "HND", -1, True, "bf16"),              # G = 3: rows 126 of 128
+    # short windows at D = 64: the one-window-tile kernel
+    ([1, 160, 64], [90, 160, 2000], 32, 2, 64, 8, "NHD", 100, False, "bf16"),  # G = 16, P = 8
+    ([300, 45], [300, 1000], 16, 2, 64, 32, "HND", 0, True, "bf16"),           # window 0, P = 32
+    ([130, 64], [500, 64], 8, 2, 64, 16, "HND", 100, True, "bf16"),            # G = 4
 ]
 
 
@@ -543,7 +547,7 @@ def test_stress_back_to_back_calls(cuda_lib, which):
 
 # ----------------------------------------------------------------- failure detection
 
-@pytest.mark.parametrize("variant", ["bf16_d128", "bf16_d64_window", "fp8", "decode_split"])
+@pytest.mark.parametrize("variant", ["bf16_d128", "bf16_d64_window", "bf16_d64_window_tile", "fp8", "decode_split"])
 def test_wait_timeout_returns_error_and_recovers(cuda_lib, variant):
     """A pipeline wait that runs out: with the stall injected, each CTA's MMA
     warp waits on a barrier that nothing arrives on, the 2 ms wait limit runs
@@ -552,6 +556,8 @@ def test_wait_timeout_returns_error_and_recovers(cuda_lib, variant):
     batch correctly with the stall off and the default limit."""
     if variant == "decode_split":
         inp = workload.build([1] * 4, [20000, 9000, 31000, 700], 32, 8, 128, 32, "HND", seed=43)
+    elif variant == "bf16_d64_window_tile":
+        inp = workload.build([200, 130], [900, 130], 16, 2, 64, 16, "HND", window_left=127, seed=42)
     else:
         D, W, kvd = {"bf16_d128": (128, -1, "bf16"), "bf16_d64_window": (64, 127, "bf16"),
                      "fp8": (128, -1, "fp8_e4m3")}[variant]
