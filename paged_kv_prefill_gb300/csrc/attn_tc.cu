@@ -604,6 +604,29 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
             float mx;
             if (interior) {
                 mx = fmax3(fmax3(mq[0], mq[1], mq[2]), mq[3], -INFINITY);
+            } else if constexpr (D == 64 && !SPLIT) {
+                // head_dim 64 (measured faster there): every key masked against the
+                // row's own range, without branches, then one maximum over the tile
+#pragma unroll
+                for (int k = 0; k < kKvTile; ++k) {
+                    const int key = k0 + k;
+                    if (key < lo || key > hi)
+                        s[k] = -INFINITY;
+                }
+                float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+                float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+                for (int k = 12; k < 120; k += 8) {
+                    m0 = fmax3(m0, s[k], s[k + 1]);
+                    m1 = fmax3(m1, s[k + 2], s[k + 3]);
+                    m2 = fmax3(m2, s[k + 4], s[k + 5]);
+                    m3 = fmax3(m3, s[k + 6], s[k + 7]);
+                }
+                m0 = fmax3(m0, s[120], s[121]);
+                m1 = fmax3(m1, s[122], s[123]);
+                m2 = fmax3(m2, s[124], s[125]);
+                m3 = fmax3(m3, s[126], s[127]);
+                mx = fmax3(fmaxf(m0, m1), m2, m3);
             } else {
                 // per 32-key chunk, decided for the whole warp: every row sees all of
                 // it (its ld.red maximum stands), no row sees any of it (maximum
@@ -661,7 +684,8 @@ __device__ void softmax_role(const AttnParams& p, const Ctx& c, int t)
                     // on a masked tile, 32 keys that no row of this warp sees give P = 0
                     // without any exponential
                     const int c0 = k0 + 2 * (part * kPartPairs + q * 16);
-                    if (!interior && __all_sync(0xffffffffu, c0 > hi || c0 + 31 < lo)) {
+                    // (head_dim 64: every chunk, its masked scores giving 0)
+                    if (!(D == 64 && !SPLIT) && !interior && __all_sync(0xffffffffu, c0 > hi || c0 + 31 < lo)) {
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk)
                             pk[kk] = 0u;
