@@ -360,7 +360,8 @@ __device__ void win_softmax(const AttnParams& p, const Ctx& c, int t)
         }
         tc_fence_after();
         // Both passes read S_t in groups of two 32-column chunks, the two
-        // loads of a group in flight together.  Per chunk, decided for the
+        // loads of a group in flight together; the loop over groups is not
+        // unrolled (measured: the smaller code runs 12 % faster).  Per chunk, decided for the
         // whole warp: every row sees all of it (its tcgen05.ld.red maximum
         // stands; plain exponentials), no row sees any of it (skipped; P = 0),
         // or masked element by element.
@@ -368,7 +369,7 @@ __device__ void win_softmax(const AttnParams& p, const Ctx& c, int t)
         constexpr int kChunks = C::kWinKeys / 32;
         // pass 1: the row maximum over the visible keys
         float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int g0 = 0; g0 < kChunks; g0 += kGroup) {
             uint32_t r[kGroup][32];
             float mq[kGroup];
@@ -394,7 +395,7 @@ __device__ void win_softmax(const AttnParams& p, const Ctx& c, int t)
         const float2 sc2 = make_float2(sl2, sl2), ng2 = make_float2(neg, neg);
         // pass 2: P = 2^(s * scale - m) for the visible keys, 0 elsewhere
         float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
+#pragma unroll 1
         for (int g0 = 0; g0 < kChunks; g0 += kGroup) {
             uint32_t r[kGroup][32];
 #pragma unroll
